@@ -1,0 +1,358 @@
+"""Benchmark: paged decode attention KV GB/s at Qwen3-4B heads on GB300.
+
+One step = one pass of the whole hot path on one layer's caches: slot
+mapping of the step's new rows, their append into the paged caches, and
+attention of every query row through the block tables.  The default
+workload is the Qwen3-4B decode step (batch 64, contexts uniform in
+[512, 4096], 32 query heads, 8 KV heads, head dim 128, block size 16,
+bf16, a shuffled pool of 20,000 blocks).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
+plain fp64 definition) on the host cores, on a bounded sample of the same
+workload.  With N > 1 (torchrun), every rank runs its own replica of the
+workload on its own GPU (no data exchange; weak scaling) and the slowest
+rank's time counts.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_mapping_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s & % of GB300 HBM peak (Qwen3-4B heads, bs 64)"
+UNIT = "GB/s"
+LAYERS = 4  # independent layer caches rotated across steps (4 x 604 MB of live KV)
+DECODE_SOURCES = ["pkv_decode.cu", "pkv_pipeline.cuh", "pkv_common.cuh"]
+
+
+# ------------------------------------------------------------------ accounting
+def step_bytes(wl, out_bytes=2):
+    """Algorithmic bytes of one step: attention reads each sequence's N_s K
+    and V rows once per KV head plus Q and writes O; the append reads the new
+    K/V rows and writes them into the caches; the slot step and the tables
+    are listed separately."""
+    eb = {"f32": 4, "bf16": 2, "e4m3": 1}[wl.kv]
+    sb = 4 if wl.src == "f32" else 2
+    kv = wl.kv_bytes_read()
+    q = wl.T * wl.Hq * wl.D * sb
+    o = wl.T * wl.Hq * wl.D * out_bytes
+    app = wl.T * wl.Hkv * wl.D * 2 * (sb + eb)
+    tables = int(sum(-(-int(n) // wl.block_size) for n in wl.seq_lens)) * 4 + wl.B * 8
+    return {"attention": kv + q + o, "kv": kv, "q": q, "o": o, "append": app, "tables": tables,
+            "total": kv + q + o + app}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != decode_source_hash():
+        return None
+    return rec
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_mapping_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import torch
+
+    from paged_kv_cache_mapping_gb300 import (harness, pkv_append, pkv_attention, pkv_device_errors,
+                                              pkv_slot_mapping)
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = W.qwen3_4b_decode(seed=1002 + 100 * rank)
+    ds = harness.DeviceStep(wl, device=dev, out_dtype=torch.bfloat16, layers=LAYERS, max_q_len=1)
+    torch.cuda.synchronize()
+    if pkv_device_errors(dev) != 0:
+        raise RuntimeError("device error flags set during set-up")
+    nb = step_bytes(wl)
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        ds.step(i % LAYERS)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            layer = i % LAYERS
+            e0, e1, e2 = ev[i]
+            kc, vc = ds.caches[layer]
+            e0.record(stream)
+            pkv_slot_mapping(ds.cu_q, ds.seq_lens, ds.bt, wl.block_size, out=ds.slots)
+            pkv_append(ds.k_new, ds.v_new, ds.slots, kc, vc, wl.k_scale, wl.v_scale)
+            e1.record(stream)
+            pkv_attention(ds.q, ds.cu_q, ds.seq_lens, ds.bt, kc, vc, wl.scale, ds.out, wl.k_scale,
+                          wl.v_scale, 1, ds.ws)
+            e2.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    flags = pkv_device_errors(dev)
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x} in the timed region")
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = [e1.elapsed_time(e2) for e0, e1, e2 in ev]
+    ms_step = total_ms / args.steps
+
+    # slowest rank
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    e2e = run_e2e(ds, wl, nb, args, dev, world)
+    if rank != 0:
+        return None
+    hbm, peak_kind = peaks()
+    attn_avg_ms = statistics.mean(attn_ms)
+    achieved = nb["attention"] / (attn_avg_ms * 1e-3) / 1e9
+    rec = traffic_record()
+    value = nb["total"] * world / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64, N(0,1) rounded to bf16)",
+        "config": {"workload": wl.name, "batch": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                   "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+                   "mean_ctx": float(wl.seq_lens.mean()), "out_dtype": "bf16",
+                   "step": "slot mapping + append + attention (one layer)",
+                   "l2": f"inputs larger than L2: {LAYERS} layer caches rotated, "
+                         f"{nb['kv'] / 1e6:.0f} MB of live KV each",
+                   "bytes_per_step": nb, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "pkv_attention (plan + decode kernels)",
+                     "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": rec["dram_bytes_per_launch"] if rec else None,
+                     "algorithmic_bytes": nb["attention"], "avg_launch_us": round(attn_avg_ms * 1e3, 2)},
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, nb, budget_s=args.cpu_budget)
+    return line
+
+
+def run_e2e(ds, wl, nb, args, dev, world):
+    """Same metric through the public API with host buffers: every step
+    copies the step's inputs from pinned host memory and reads the output
+    back."""
+    import torch
+
+    from paged_kv_cache_mapping_gb300 import pkv_append, pkv_attention, pkv_slot_mapping
+    host = {k: v.cpu().pin_memory() for k, v in
+            (("q", ds.q), ("k", ds.k_new), ("v", ds.v_new), ("cu", ds.cu_q), ("sl", ds.seq_lens),
+             ("bt", ds.bt))}
+    dst = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one(i):
+        for k in host:
+            dst[k].copy_(host[k], non_blocking=True)
+        kc, vc = ds.caches[i % LAYERS]
+        pkv_slot_mapping(dst["cu"], dst["sl"], dst["bt"], wl.block_size, out=ds.slots)
+        pkv_append(dst["k"], dst["v"], ds.slots, kc, vc, wl.k_scale, wl.v_scale)
+        pkv_attention(dst["q"], dst["cu"], dst["sl"], dst["bt"], kc, vc, wl.scale, ds.out, wl.k_scale,
+                      wl.v_scale, 1, ds.ws)
+        out_h.copy_(ds.out, non_blocking=True)
+
+    for i in range(args.warmup):
+        one(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(args.steps):
+        one(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(nb["total"] * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ oracle
+def cpu_baseline(wl, nb, budget_s=20.0, nthreads=None):
+    """The oracle as it stands, on the host cores: its cache is built once
+    (untimed), then whole steps (slot mapping, append of the new rows,
+    attention of every row) are timed until the budget is spent."""
+    import oracle
+
+    nthreads = nthreads or oracle.cpu_count()
+    kc = np.zeros(wl.cache_shape(), wl.cache_np_dtype())
+    vc = np.zeros_like(kc)
+    for s0, s1, cu, sl, k, v in wl.history_batches():
+        if k.shape[0]:
+            oracle.append(k, v, oracle.slot_mapping(cu, sl, wl.block_tables[s0:s1], wl.block_size),
+                          kc, vc, wl.k_scale, wl.v_scale)
+    kn, vn = wl.new_rows()
+    times = []
+    t_begin = time.perf_counter()
+    while not times or (time.perf_counter() - t_begin < budget_s and len(times) < 50):
+        t0 = time.perf_counter()
+        slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.seq_lens, wl.block_tables, wl.block_size)
+        oracle.append(kn, vn, slots, kc, vc, wl.k_scale, wl.v_scale)
+        oracle.attention(wl.q, wl.cu_seqlens_q, wl.seq_lens, wl.block_tables, kc, vc, wl.scale, wl.k_scale,
+                         wl.v_scale, nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+    per = statistics.median(times)
+    return {"value": round(nb["total"] / per / 1e9, 3), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(times)} whole steps of the same workload (all {wl.T} query rows), "
+                      f"median {per * 1e3:.1f} ms per step, fp64, {nthreads} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = W.qwen3_4b_decode(seed=1002)
+    nb = step_bytes(wl)
+    cb = cpu_baseline(wl, nb, budget_s=args.cpu_budget)
+    per_s = nb["total"] / (cb["value"] * 1e9)
+    return {"metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(per_s * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl.name, "batch": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                       "block_size": wl.block_size},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ main
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N > 1 with torch.distributed.run")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl")
+        line = run_ours(args, rank, world)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

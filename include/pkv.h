@@ -1,0 +1,217 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: paged KV cache append and attention for one
+ * GB300 (sm_103a) GPU.
+ *
+ * The problem, as the pages state it:
+ *   - "How to design an LLM serving system (a vLLM deep dive)", section
+ *     "PagedAttention (vLLM KV manager)": the KV cache is a pool of fixed
+ *     physical blocks of block_size tokens; each request's block table maps
+ *     its logical positions to non-contiguous physical blocks; slot_mapping
+ *     tells the kernel which physical slot each token's K/V goes to.
+ *   - nanoserve, section "Architecture" (one engine step): all new tokens of
+ *     a step are packed into one [T] dimension, each token's cache slot is
+ *     computed from its block table (step 2), and each layer writes this
+ *     step's K/V into the paged cache, then attends over the full context
+ *     through the block table (step 3); decodes and prefill chunks share a
+ *     step ("Chunked prefill", "Packed batches").
+ *   - "How Easy Is It to Start Serving LLMs?", section "1. Block-sparse KV
+ *     memory": the page table is all the attention kernel needs; pages may
+ *     sit anywhere in the pool and may be shared.
+ *
+ * Layouts (row-major, innermost last):
+ *   q, out        [T, Hq, D]        packed query rows of all sequences
+ *   k, v          [T, Hkv, D]       this step's new K/V rows
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, Hkv, D]   one layer, contiguous
+ *   block_tables  [B, max_blocks]   int32 physical block ids
+ *   cu_seqlens_q  [B+1]             int32, rows of sequence s are
+ *                                   cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1
+ *   seq_lens      [B]               int32, N_s = keys of sequence s, this
+ *                                   step's new tokens included
+ *   slot_mapping  [T]               int32 or int64 flat slot per new row
+ *
+ * Semantics (every function):
+ *   - Query row i of sequence s (q_s = cu_seqlens_q[s+1]-cu_seqlens_q[s]
+ *     rows) sits at position p = N_s - q_s + i and attends, causally, to
+ *     keys 0..p; a decode is the q_s = 1 case.  Query head h reads KV head
+ *     h / (Hq / Hkv).
+ *   - The flat slot of position p is
+ *     block_tables[s][p / block_size] * block_size + p % block_size, and
+ *     slot = block * block_size + offset addresses
+ *     cache[block][offset][head][:].
+ *   - fp8 caches hold OCP e4m3 codes of x / scale (per-tensor scales).
+ *
+ * Ownership and execution: the caller owns every buffer (device memory,
+ * e.g. from PyTorch) and the stream.  The library allocates no memory and
+ * never synchronises, except in check mode (environment PKV_CHECK=1).  A
+ * PKV_OK return means the work was enqueued on the stream.  Pointers are
+ * device pointers unless stated.  Device-resident indices (slots, block
+ * ids, lengths) are bounds-checked by the kernels: an out-of-range index
+ * is skipped (no write, zero contribution) and recorded; check mode, or
+ * pkv_device_errors(), reports it.  No kernel traps or faults on bad
+ * indices.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the library are exported; everything else in it is hidden. */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARGUMENT = 1,    /* shapes, dtypes, strides or values disagree */
+  PKV_ERR_UNSUPPORTED = 2,         /* a valid request outside the built variants */
+  PKV_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the size required */
+  PKV_ERR_CUDA = 4,                /* a CUDA call failed; pkv_last_error() says which */
+  PKV_ERR_DEVICE_CHECK = 5         /* check mode: a kernel met an out-of-range index */
+} pkv_status;
+
+typedef enum {
+  PKV_F32 = 0,
+  PKV_BF16 = 1,
+  PKV_FP8_E4M3 = 2,
+  PKV_I32 = 3,
+  PKV_I64 = 4
+} pkv_dtype;
+
+/* A strided view of caller-owned memory.  Strides are in elements. */
+typedef struct {
+  void* data;
+  pkv_dtype dtype;
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+} pkv_tensor;
+
+/*
+ * pkv_slot_mapping -- the flat cache slot of every new row of a step.
+ * nanoserve, "Architecture", step 2 ("Prepare": compute each token's cache
+ * slot from its block table); "How to design an LLM serving system (a vLLM
+ * deep dive)", "PagedAttention" (slot_mapping).
+ *
+ *   cu_seqlens_q  [B+1] int32 (device)
+ *   seq_lens      [B]   int32 (device), N_s after this step's rows
+ *   block_tables  [B, max_blocks] int32 (device), unit column stride
+ *   block_size    tokens per block, >= 1
+ *   slot_mapping  [T] int32 or int64 (device, written), T = cu_seqlens_q[B]
+ *                 is the caller's host-side row count (shape[0])
+ *
+ * Rows of a sequence whose lengths are inconsistent (q_s < 0, q_s > N_s or
+ * N_s > max_blocks * block_size) or whose block id is negative get slot -1
+ * and are recorded as a device error.
+ */
+PKV_API pkv_status pkv_slot_mapping(const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                            const pkv_tensor* block_tables, int32_t block_size,
+                            pkv_tensor* slot_mapping, void* stream);
+
+/*
+ * pkv_append -- scatter this step's K/V rows into their slots.
+ * nanoserve, "Architecture", step 3 ("Forward": each layer writes this
+ * step's K/V into the paged cache, then attends); "How to design an LLM
+ * serving system (a vLLM deep dive)", "PagedAttention" (slot_mapping).
+ *
+ *   k, v          [T, Hkv, D], unit stride in D, 16-byte aligned rows
+ *   slot_mapping  [T] int32 or int64; a negative slot skips the row
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, Hkv, D], contiguous
+ *   k_scale,
+ *   v_scale       per-tensor scales, used only when the cache is e4m3:
+ *                 the stored code is e4m3_rn_satfinite(x * (1.0f / scale)),
+ *                 the product taken in fp32 ("How Easy Is It to Start
+ *                 Serving LLMs?", "What each setting does to performance":
+ *                 FP8 KV cache)
+ *
+ * Supported: f32 -> f32, bf16 -> bf16, bf16 or f32 -> e4m3; D a multiple of
+ * 8 up to 256.  Same-format rows are copied bit for bit.  Slots at or beyond
+ * num_blocks * block_size are skipped and recorded.  Two rows with the same
+ * non-negative slot in one call leave that slot unspecified.
+ */
+PKV_API pkv_status pkv_append(const pkv_tensor* k, const pkv_tensor* v, const pkv_tensor* slot_mapping,
+                      pkv_tensor* k_cache, pkv_tensor* v_cache, float k_scale, float v_scale,
+                      void* stream);
+
+/*
+ * pkv_attention_workspace_size -- bytes of device workspace pkv_attention
+ * needs for these shapes (a host-side bound; no device access).
+ *   q [T, Hq, D], block_tables [B, max_blocks], k_cache [NB, bs, Hkv, D].
+ */
+PKV_API pkv_status pkv_attention_workspace_size(const pkv_tensor* q, const pkv_tensor* block_tables,
+                                        const pkv_tensor* k_cache, size_t* bytes);
+
+/*
+ * pkv_attention -- causal GQA attention of the packed query rows over each
+ * sequence's pages.
+ * nanoserve, "Architecture" step 3 and the "Triton paged-attention decode
+ * kernel" bullet (K/V read straight from the block table with an online
+ * softmax, decodes and prefill chunks in one step); "How Easy Is It to Start
+ * Serving LLMs?", "3. Load balancing: keep every SM busy" (long requests are
+ * split into chunks and a merge step stitches them back together).
+ *
+ *   q             [T, Hq, D] bf16 or f32, unit stride in D
+ *   cu_seqlens_q  [B+1] int32
+ *   seq_lens      [B] int32 (N_s includes this step's rows)
+ *   block_tables  [B, max_blocks] int32, unit column stride; entries past
+ *                 ceil(N_s / block_size) are never read
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, Hkv, D] contiguous; bf16 or e4m3
+ *                 with bf16 q, f32 with f32 q
+ *   scale         softmax scale (e.g. 1/sqrt(D))
+ *   k_scale,
+ *   v_scale       e4m3 dequantisation scales (value = code * scale); ignored
+ *                 for bf16/f32 caches
+ *   max_q_len     a host-side upper bound on q_s (1 for a pure decode batch;
+ *                 <= 0 means "unknown", taken as T).  With max_q_len == 1
+ *                 only the decode path is launched.
+ *   out           [T, Hq, D] f32 or bf16 (written), unit stride in D
+ *   workspace     device scratch of workspace_bytes, at least
+ *                 pkv_attention_workspace_size(); 256-byte aligned
+ *
+ * The result for a row depends only on its own sequence (lengths, pages'
+ * contents, query), never on the block size, the physical placement of
+ * pages, or the other sequences of the batch: all tiling and splitting is
+ * in logical token positions.  A bf16 output equals the f32 output rounded
+ * to nearest even.
+ *
+ * Supported: Hq % Hkv == 0; D in {64, 128} for bf16/e4m3 caches, D a
+ * multiple of 32 up to 256 for f32 caches; any block_size >= 1; q_s = 0
+ * sequences produce no rows.
+ */
+PKV_API pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
+                         const pkv_tensor* seq_lens, const pkv_tensor* block_tables,
+                         const pkv_tensor* k_cache, const pkv_tensor* v_cache, float scale,
+                         float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_device_errors -- synchronise the stream, then return (in *flags) and
+ * clear the record of out-of-range indices the kernels met on the current
+ * device since the last call.  Bits: 1 = slot beyond the pool, 2 = block id
+ * out of range, 4 = inconsistent lengths, 8 = a bounded wait gave up.
+ */
+PKV_API pkv_status pkv_device_errors(void* stream, uint32_t* flags);
+
+/* Static description of a status code. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+PKV_API const char* pkv_last_error(void);
+
+/* Library version, "major.minor.patch". */
+PKV_API const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,87 @@
+// pkv_kernels.h -- parameter blocks and launchers shared between the host
+// side of libpkv (pkv_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// ---------------------------------------------------------------- append
+struct AppendParams {
+  const void* k;
+  const void* v;
+  int64_t k_st, k_sh, v_st, v_sh;  // row strides (elements) of k and v
+  const void* slots;               // int32 or int64 [T]
+  void* k_cache;
+  void* v_cache;
+  int64_t T;
+  int32_t Hkv, D;
+  int64_t num_slots;  // num_blocks * block_size
+  float k_inv_scale, v_inv_scale;
+  unsigned int* err;
+};
+
+cudaError_t launch_slot_mapping(const int32_t* cu_q, const int32_t* seq_lens, const int32_t* bt,
+                                int64_t bt_stride, int32_t max_blocks, int32_t B, int32_t bs, void* slots,
+                                bool slots_i64, int64_t T, unsigned int* err, cudaStream_t stream);
+
+// src_kind: 0 = f32 rows, 1 = bf16 rows.
+cudaError_t launch_append(const AppendParams& p, int src_kind, bool fp8, bool slots_i64,
+                          cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+// Device workspace of one attention call (all offsets 256-byte aligned).
+struct Workspace {
+  int32_t* dec_off;    // [B+1] prefix sums of decode chunk units
+  int32_t* pf_off;     // [B+1] prefix sums of prefill row tiles
+  int32_t* counters;   // [B * Hkv] chunks finished per (sequence, KV head)
+  float* part_o;       // [B * kMaxChunks, Hq, D] chunk outputs (normalised)
+  float* part_lse;     // [B * kMaxChunks, Hq] chunk log2-sum-exp2
+};
+
+struct AttnParams {
+  // query rows and output
+  const void* q;
+  int64_t q_st, q_sh;  // strides (elements)
+  void* out;
+  int64_t o_st, o_sh;
+  // sequences
+  int64_t T;  // packed query rows (host-side count; cu_seqlens_q must stay within it)
+  const int32_t* cu_q;
+  const int32_t* seq_lens;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int32_t max_blocks;
+  int32_t B;
+  // caches [num_blocks, bs, Hkv, D]
+  const void* k_cache;
+  const void* v_cache;
+  int64_t num_blocks;
+  int32_t bs;
+  int32_t bs_shift;  // log2(bs) when bs is a power of two, else -1
+  int32_t Hq, Hkv, G, D;
+  float qk_scale_log2;  // scale * k_scale * log2(e)
+  float v_scale;        // applied to the output (e4m3 caches), else 1
+  int32_t decode_max_g;  // sequences with q_s == 1 and G <= this take the decode path
+  Workspace ws;
+  unsigned int* err;
+};
+
+// Launchers.  out_kind: 0 = f32, 1 = bf16.  kv: 0 = f32, 1 = bf16, 2 = e4m3.
+size_t attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t D);
+
+// Raises a kernel's dynamic shared memory limit once per device.
+cudaError_t set_smem_attr(const void* kernel, size_t bytes);
+
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_prefill(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_f32(const AttnParams& p, int out_kind, int64_t T, cudaStream_t st);
+
+}  // namespace pkv
