@@ -33,7 +33,9 @@ from paged_kv_cache_mapping_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s & % of GB300 HBM peak (Qwen3-4B heads, bs 64)"
 UNIT = "GB/s"
-LAYERS = 4  # independent layer caches rotated across steps (4 x 604 MB of live KV)
+WORKLOADS = ("decode", "layout-bs1-scattered", "layout-bs1-contiguous", "layout-bs16-scattered",
+             "layout-bs16-contiguous", "layout-bs64-scattered", "layout-bs64-contiguous", "mixed",
+             "long-fp8", "lognormal-fp8")
 DECODE_SOURCES = ["pkv_decode.cu", "pkv_pipeline.cuh", "pkv_common.cuh"]
 
 
@@ -152,8 +154,10 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    wl = W.qwen3_4b_decode(seed=1002 + 100 * rank)
-    ds = harness.DeviceStep(wl, device=dev, out_dtype=torch.bfloat16, layers=LAYERS, max_q_len=1)
+    LAYERS = args.layers
+    wl = make_workload(args.workload, rank)
+    max_q = int(wl.q_lens.max())
+    ds = harness.DeviceStep(wl, device=dev, out_dtype=torch.bfloat16, layers=LAYERS, max_q_len=max_q)
     torch.cuda.synchronize()
     if pkv_device_errors(dev) != 0:
         raise RuntimeError("device error flags set during set-up")
@@ -182,7 +186,7 @@ def run_ours(args, rank, world):
             pkv_append(ds.k_new, ds.v_new, ds.slots, kc, vc, wl.k_scale, wl.v_scale)
             e1.record(stream)
             pkv_attention(ds.q, ds.cu_q, ds.seq_lens, ds.bt, kc, vc, wl.scale, ds.out, wl.k_scale,
-                          wl.v_scale, 1, ds.ws)
+                          wl.v_scale, max_q, ds.ws)
             e2.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -199,7 +203,7 @@ def run_ours(args, rank, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
 
-    e2e = run_e2e(ds, wl, nb, args, dev, world)
+    e2e = run_e2e(ds, wl, nb, args, dev, world, max_q)
     if rank != 0:
         return None
     hbm, peak_kind = peaks()
@@ -216,7 +220,7 @@ def run_ours(args, rank, world):
                    "block_size": wl.block_size, "num_blocks": wl.num_blocks,
                    "mean_ctx": float(wl.seq_lens.mean()), "out_dtype": "bf16",
                    "step": "slot mapping + append + attention (one layer)",
-                   "l2": f"inputs larger than L2: {LAYERS} layer caches rotated, "
+                   "l2": f"inputs larger than L2: {LAYERS} layer cache(s) rotated, "
                          f"{nb['kv'] / 1e6:.0f} MB of live KV each",
                    "bytes_per_step": nb, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": "pkv_attention (plan + decode kernels)",
@@ -225,7 +229,7 @@ def run_ours(args, rank, world):
                      "traffic": rec["dram_bytes_per_launch"] if rec else None,
                      "algorithmic_bytes": nb["attention"], "avg_launch_us": round(attn_avg_ms * 1e3, 2)},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (5 if max_q > 1 else 4) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -233,7 +237,7 @@ def run_ours(args, rank, world):
     return line
 
 
-def run_e2e(ds, wl, nb, args, dev, world):
+def run_e2e(ds, wl, nb, args, dev, world, max_q):
     """Same metric through the public API with host buffers: every step
     copies the step's inputs from pinned host memory and reads the output
     back."""
@@ -252,11 +256,11 @@ def run_e2e(ds, wl, nb, args, dev, world):
     def one(i):
         for k in host:
             dst[k].copy_(host[k], non_blocking=True)
-        kc, vc = ds.caches[i % LAYERS]
+        kc, vc = ds.caches[i % len(ds.caches)]
         pkv_slot_mapping(dst["cu"], dst["sl"], dst["bt"], wl.block_size, out=ds.slots)
         pkv_append(dst["k"], dst["v"], ds.slots, kc, vc, wl.k_scale, wl.v_scale)
         pkv_attention(dst["q"], dst["cu"], dst["sl"], dst["bt"], kc, vc, wl.scale, ds.out, wl.k_scale,
-                      wl.v_scale, 1, ds.ws)
+                      wl.v_scale, max_q, ds.ws)
         out_h.copy_(ds.out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -307,10 +311,27 @@ def cpu_baseline(wl, nb, budget_s=20.0, nthreads=None):
                       f"median {per * 1e3:.1f} ms per step, fp64, {nthreads} threads"}
 
 
+def make_workload(name, rank=0):
+    """The benchmark workloads (seeded per rank: each rank owns a replica)."""
+    off = 100 * rank
+    if name == "decode":
+        return W.qwen3_4b_decode(seed=1002 + off)
+    if name.startswith("layout-"):
+        _, bs, lay = name.split("-")
+        return W.layout_sweep(int(bs[2:]), lay == "contiguous", seed=1003 + off)
+    if name == "mixed":
+        return W.mixed_prefill(seed=1004 + off)
+    if name == "long-fp8":
+        return W.long_fp8(seed=1005 + off)
+    if name == "lognormal-fp8":
+        return W.lognormal_fp8(seed=1006 + off)
+    raise ValueError(name)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    wl = W.qwen3_4b_decode(seed=1002)
+    wl = make_workload(args.workload)
     nb = step_bytes(wl)
     cb = cpu_baseline(wl, nb, budget_s=args.cpu_budget)
     per_s = nb["total"] / (cb["value"] * 1e9)
@@ -331,6 +352,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default="decode")
+    ap.add_argument("--layers", type=int, default=4, help="layer caches rotated across steps")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

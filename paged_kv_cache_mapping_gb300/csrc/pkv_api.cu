@@ -13,7 +13,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 #include "pkv_kernels.h"
 
 namespace {
@@ -220,14 +220,33 @@ cudaError_t set_smem_attr(const void* kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-size_t attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t D) {
+static int64_t max_prefill_tiles(int64_t B, int64_t T, int64_t G) {
+  return (T * G + kPrefillRows - 1) / kPrefillRows + B;
+}
+
+struct WsLayout {
+  size_t dec_off, pf_off, counters, work, dec_desc, pf_desc, part_o, part_lse, total;
+};
+
+static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_ctx) {
+  const int64_t G = Hkv > 0 ? Hq / Hkv : 1;
+  const int64_t units = B * max_chunks_for(max_ctx);
+  WsLayout L{};
   size_t n = 0;
-  n += align_up(sizeof(int32_t) * (B + 1), 256);      // dec_off
-  n += align_up(sizeof(int32_t) * (B + 1), 256);      // pf_off
-  n += align_up(sizeof(int32_t) * B * Hkv, 256);      // counters
-  n += align_up(sizeof(float) * B * kMaxChunks * Hq * D, 256);  // part_o
-  n += align_up(sizeof(float) * B * kMaxChunks * Hq, 256);      // part_lse
-  return n;
+  L.dec_off = n;  n += align_up(sizeof(int32_t) * (B + 1), 256);
+  L.pf_off = n;   n += align_up(sizeof(int32_t) * (B + 1), 256);
+  L.counters = n; n += align_up(sizeof(int32_t) * B * Hkv, 256);
+  L.work = n;     n += 256;
+  L.dec_desc = n; n += align_up(sizeof(DecodeDesc) * units, 256);
+  L.pf_desc = n;  n += align_up(sizeof(PrefillDesc) * max_prefill_tiles(B, T, G), 256);
+  L.part_o = n;   n += align_up(sizeof(float) * units * Hq * D, 256);
+  L.part_lse = n; n += align_up(sizeof(float) * units * Hq, 256);
+  L.total = n;
+  return L;
+}
+
+size_t attention_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_ctx) {
+  return ws_layout(B, T, Hq, Hkv, D, max_ctx).total;
 }
 
 }  // namespace pkv
@@ -367,7 +386,9 @@ pkv_status pkv_attention_workspace_size(const pkv_tensor* q, const pkv_tensor* b
   PKV_TRY(check_tensor("block_tables", block_tables, 2));
   PKV_TRY(check_tensor("k_cache", k_cache, 4));
   PKV_TRY(need(bytes != nullptr, "bytes is NULL"));
-  *bytes = pkv::attention_workspace_bytes(block_tables->shape[0], q->shape[1], k_cache->shape[2], q->shape[2]);
+  PKV_TRY(need(k_cache->shape[2] >= 1, "Hkv must be >= 1"));
+  *bytes = pkv::attention_workspace_bytes(block_tables->shape[0], q->shape[0], q->shape[1], k_cache->shape[2],
+                                          q->shape[2], block_tables->shape[1] * k_cache->shape[1]);
   return PKV_OK;
 }
 
@@ -418,7 +439,8 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
     PKV_TRY(need(k_scale > 0.f && v_scale > 0.f && k_scale == k_scale && v_scale == v_scale,
                  "fp8 scales must be positive and finite"));
   PKV_TRY(need(scale == scale, "scale is NaN"));
-  const size_t ws_need = pkv::attention_workspace_bytes(B, Hq, Hkv, D);
+  const int64_t max_ctx = block_tables->shape[1] * bs;
+  const size_t ws_need = pkv::attention_workspace_bytes(B, T, Hq, Hkv, D, max_ctx);
   if (kv != 0) {
     if (workspace_bytes < ws_need)
       return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace needs " + std::to_string(ws_need) + " bytes, got " +
@@ -467,32 +489,30 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
     return finish(st, "pkv_attention");
   }
   // workspace carve-up
-  char* w = static_cast<char*>(workspace);
-  p.ws.dec_off = reinterpret_cast<int32_t*>(w);
-  w += align_up(sizeof(int32_t) * (B + 1), 256);
-  p.ws.pf_off = reinterpret_cast<int32_t*>(w);
-  w += align_up(sizeof(int32_t) * (B + 1), 256);
-  p.ws.counters = reinterpret_cast<int32_t*>(w);
-  w += align_up(sizeof(int32_t) * B * Hkv, 256);
-  p.ws.part_o = reinterpret_cast<float*>(w);
-  w += align_up(sizeof(float) * B * pkv::kMaxChunks * Hq * D, 256);
-  p.ws.part_lse = reinterpret_cast<float*>(w);
-
+  {
+    const pkv::WsLayout L = pkv::ws_layout(B, T, Hq, Hkv, D, max_ctx);
+    char* w = static_cast<char*>(workspace);
+    p.ws.dec_off = reinterpret_cast<int32_t*>(w + L.dec_off);
+    p.ws.pf_off = reinterpret_cast<int32_t*>(w + L.pf_off);
+    p.ws.counters = reinterpret_cast<int32_t*>(w + L.counters);
+    p.ws.work = reinterpret_cast<int32_t*>(w + L.work);
+    p.ws.dec_desc = reinterpret_cast<pkv::DecodeDesc*>(w + L.dec_desc);
+    p.ws.pf_desc = reinterpret_cast<pkv::PrefillDesc*>(w + L.pf_desc);
+    p.ws.part_o = reinterpret_cast<float*>(w + L.part_o);
+    p.ws.part_lse = reinterpret_cast<float*>(w + L.part_lse);
+  }
   const int G = p.G;
   const bool prefill = (max_q_len > 1) || (max_q_len <= 0 && T >= 2) || G > p.decode_max_g;
   e = pkv::launch_plan(p, st);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   if (prefill) {
-    const int64_t tiles = (T * G + pkv::kPrefillRows - 1) / pkv::kPrefillRows + B;
+    const int64_t tiles = pkv::max_prefill_tiles(B, T, G);
     e = pkv::launch_prefill(p, kv, out_kind, tiles * Hkv, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (G <= p.decode_max_g) {
-    const int64_t maxctx = block_tables->shape[1] * bs;
-    const int ct = pkv::chunk_tokens(static_cast<int>(maxctx));
-    const int64_t max_chunks = (maxctx + ct - 1) / ct;
     const int64_t dec_seqs = std::min<int64_t>(B, T);
-    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * max_chunks * Hkv, sms, st);
+    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * pkv::max_chunks_for(max_ctx) * Hkv, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return finish(st, "pkv_attention");

@@ -26,17 +26,24 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 
 // Logical tiling.  Every tile and split boundary is a logical token position
 // so that the result does not depend on block_size or page placement.
-constexpr int kStageTokens = 64;      // K/V rows per pipeline stage
-constexpr int kChunkBase = 512;       // smallest split-KV chunk (tokens)
-constexpr int kMaxChunks = 32;        // a sequence is split into at most this many chunks
+constexpr int kChunkBase = 256;       // smallest split-KV chunk (tokens)
+constexpr int kMaxChunks = 128;       // a sequence is split into at most this many chunks
 constexpr int kPrefillRows = 64;      // (query token, head) rows per prefill tile
 
-// Chunk length of a decoding sequence of n keys: the smallest 512 * 2^k
+// Chunk length of a decoding sequence of n keys: the smallest 256 * 2^k
 // that splits it into at most kMaxChunks chunks.  Depends on n only.
 __host__ __device__ inline int chunk_tokens(int n) {
   int64_t c = kChunkBase;
   while (((int64_t)n + c - 1) / c > kMaxChunks) c <<= 1;
   return static_cast<int>(c);
+}
+
+// Chunks of the longest sequence a block table of max_ctx tokens can hold.
+__host__ __device__ inline int max_chunks_for(int64_t max_ctx) {
+  if (max_ctx <= 0) return 1;
+  const int n = max_ctx > 0x7fffffff ? 0x7fffffff : static_cast<int>(max_ctx);
+  const int c = chunk_tokens(n);
+  return (n + c - 1) / c;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

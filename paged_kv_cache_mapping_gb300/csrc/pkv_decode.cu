@@ -8,34 +8,42 @@
 // LLMs?", "1. Block-sparse KV memory").
 //
 // Design (GB300):
-//   * Persistent CTAs, one work item = (sequence, logical chunk, KV head).
-//     The chunk length depends only on N_s (512 * 2^k tokens, at most 32
-//     chunks), so results do not depend on the batch or the page layout
+//   * A work item is (sequence, logical chunk, group of HP KV heads).  The
+//     chunk length depends only on N_s (256 * 2^k tokens, at most 128
+//     chunks), so results depend neither on the batch nor on the page layout
 //     ("How Easy Is It to Start Serving LLMs?", "3. Load balancing": long
-//     requests are split into chunks and a merge step stitches them).
-//   * One producer warp copies each K and V row (one token, one KV head,
-//     D elements) from its page into shared memory with a 1-D bulk copy
-//     (TMA) that completes on an mbarrier; stages of 64 logical tokens form
-//     a ring.  Every page is read once for all Hq/Hkv query heads.
-//   * Four consumer warps each take 16 tokens of a stage.  S = K q^T and
-//     O^T += V^T P run on the tensor cores (mma.sync m16n8k16): the keys are
-//     the M dimension and the group's query heads the N dimension, so the
-//     softmax statistics of a head live in one lane column.  P is fed to
-//     the PV product as a bf16 hi + lo pair (two MMAs), which keeps it to
-//     about 16 significant bits; with an e4m3 cache, K and V are converted
-//     exactly to f16 and P is f16.
-//   * Each warp keeps its own running max and sum; the four are combined at
-//     the end of the chunk in a fixed order.  A sequence of one chunk writes
-//     its output directly; otherwise each chunk writes its normalised output
-//     and log2-sum-exp2 to the workspace, and the CTA that finishes the last
-//     chunk of a (sequence, KV head) merges them (no separate merge launch).
+//     requests are split into chunks and a merge step stitches them).  The
+//     plan kernel lists the chunks once per call; persistent CTAs (one per
+//     SM) claim items from a global counter, so every SM stays busy to the
+//     end.
+//   * One producer warp per CTA stages the chunk 16 logical tokens at a time:
+//     a token's K row for all HP heads of the group is HP * D contiguous
+//     elements of the cache (2 KB at D = 128, bf16, HP = 8), fetched with one
+//     1-D bulk copy (TMA) that completes on the stage's mbarrier; V likewise.
+//     Whole-token copies keep the number of TMA requests low, which is what
+//     limits a TMA gather of small rows.  Block ids are fetched a stage
+//     ahead; the item's descriptor and query rows go through a two-slot item
+//     ring.  Every page is read once for all Hq/Hkv query heads.
+//   * Consumer warp h owns KV head h of the group for the whole chunk: S =
+//     K q^T and O^T += V^T P run on the tensor cores (mma.sync m16n8k16)
+//     with the 16 keys of a stage as M and the head's G query heads as N, so
+//     a head's softmax statistics live in one lane column and need no
+//     cross-warp combine.  P enters the PV product as a bf16 hi + lo pair
+//     (two MMAs; about 16 significant bits); with an e4m3 cache K and V are
+//     converted exactly to f16 and P is f16.
+//   * A sequence of one chunk writes its output directly.  Otherwise each
+//     chunk writes its normalised output and log2-sum-exp2 to the workspace,
+//     and the warp that finishes the last chunk of a (sequence, KV head)
+//     merges them in chunk order (no separate merge launch, no CTA-wide
+//     synchronisation).
 #include "pkv_pipeline.cuh"
 
 namespace pkv {
 
 // ---------------------------------------------------------------- plan
-// One block: per-sequence work counts, their exclusive prefix sums, and the
-// merge counters reset.  Reads device lengths; no host round trip.
+// One block: per-sequence work counts, their exclusive prefix sums, the
+// descriptor lists of decode chunks and prefill tiles, and the merge
+// counters reset.  Reads device lengths; no host round trip.
 __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   __shared__ int warp_d[32], warp_p[32];
   const int tid = threadIdx.x, nth = blockDim.x;
@@ -106,6 +114,38 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     counts(s, d, f);
     p.ws.dec_off[s] = run_d;
     p.ws.pf_off[s] = run_p;
+    const int n = __ldg(p.seq_lens + s);
+    const int t0 = __ldg(p.cu_q + s);
+    if (d > 0) {
+      const int ct = chunk_tokens(n);
+      for (int c = 0; c < d; ++c) {
+        DecodeDesc e;
+        e.s = s;
+        e.k0 = c * ct;
+        e.k1 = min(e.k0 + ct, n);
+        e.t = t0;
+        e.nchunks = d;
+        e.u0 = run_d;
+        e.c = c;
+        e.pad = 0;
+        p.ws.dec_desc[run_d + c] = e;
+      }
+    }
+    if (f > 0) {
+      const int q_s = __ldg(p.cu_q + s + 1) - t0;
+      for (int qt = 0; qt < f; ++qt) {
+        PrefillDesc e;
+        e.s = s;
+        e.t0 = t0;
+        e.q_s = q_s;
+        e.n = n;
+        e.r0 = qt * kPrefillRows;
+        e.r1 = min(e.r0 + kPrefillRows, q_s * p.G);
+        e.kv_end = n - q_s + (e.r1 - 1) / p.G + 1;
+        e.pad = 0;
+        p.ws.pf_desc[run_p + qt] = e;
+      }
+    }
     run_d += d;
     run_p += f;
   }
@@ -118,44 +158,34 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     p.ws.pf_off[0] = 0;
   }
   for (int i = tid; i < B * p.Hkv; i += nth) p.ws.counters[i] = 0;
+  if (tid == 0) *p.ws.work = 0;
 }
 
 // ---------------------------------------------------------------- decode
 template <int KV, int D>
-struct DecodeCfg {
-  static constexpr int kEsz = KV == 2 ? 1 : 2;       // bytes per cache element
-  static constexpr int kRowB = D * kEsz;              // bytes per K/V row
-  static constexpr int kRowS = kRowB + 16;            // padded smem row stride
-  static constexpr int kNW = 4;                       // consumer warps
-  static constexpr int kST = 16 * kNW;                // tokens per stage
-  static constexpr int kNS = KV == 2 ? 6 : 4;         // stages in the ring
-  static constexpr int kStageB = 2 * kST * kRowS;     // K rows then V rows
-  static constexpr int kMT = D / 16;                  // 16-wide d tiles
-  static constexpr int kThreads = (kNW + 1) * 32;
-  // combine area: m[kNW][8], l[kNW][8], o[kNW][8][D], merge weights [8][kMaxChunks]
-  static constexpr int kCombFloats = kNW * 8 * 2 + kNW * 8 * D + 8 * kMaxChunks;
-  static constexpr size_t kSmem = (size_t)kNS * kStageB + kCombFloats * 4 + 2 * kNS * 8 + 64;
+struct DecodeGeom {
+  static constexpr int kRowB = D * (KV == 2 ? 1 : 2);  // one head's K (or V) row
+  static constexpr int kST = 16;                        // tokens per stage
+  static constexpr int kMT = D / 16;                    // 16-wide tiles over d
+  static constexpr int kQRowB = D * 2;                  // one bf16 query row
+  static constexpr int kMaxHP = 8;
+  static constexpr int kThreads = (kMaxHP + 1) * 32;
 };
 
-struct DecodeItem {
-  int s, c, g, nchunks, k0, k1, u;
-  int64_t t;
-};
+__host__ __device__ inline int align16(int v) { return (v + 15) & ~15; }
 
-__device__ __forceinline__ bool decode_item(const AttnParams& p, int w, DecodeItem& it) {
-  const int units = __ldg(p.ws.dec_off + p.B);
-  if (w >= units * p.Hkv) return false;
-  it.u = w / p.Hkv;
-  it.g = w - it.u * p.Hkv;
-  it.s = upper_index(p.ws.dec_off, p.B, it.u);
-  it.c = it.u - __ldg(p.ws.dec_off + it.s);
-  const int n = __ldg(p.seq_lens + it.s);
-  const int ct = chunk_tokens(n);
-  it.nchunks = (n + ct - 1) / ct;
-  it.k0 = it.c * ct;
-  it.k1 = min(it.k0 + ct, n);
-  it.t = __ldg(p.cu_q + it.s);
-  return true;
+// Shared memory of a decode CTA: the stage ring, the item ring, mbarriers.
+template <int KV, int D>
+__host__ __device__ inline int decode_tok_stride(int hp) { return hp * DecodeGeom<KV, D>::kRowB + 16; }
+template <int KV, int D>
+__host__ __device__ inline int decode_stage_bytes(int hp) { return 2 * DecodeGeom<KV, D>::kST * decode_tok_stride<KV, D>(hp); }
+template <int KV, int D>
+__host__ __device__ inline int decode_item_bytes(int hp, int G) {
+  return align16(hp * G * DecodeGeom<KV, D>::kQRowB + 64);
+}
+template <int KV, int D>
+__host__ __device__ inline size_t decode_smem(int hp, int ns, int G) {
+  return (size_t)ns * decode_stage_bytes<KV, D>(hp) + 2 * decode_item_bytes<KV, D>(hp, G) + (2 * ns + 4) * 8 + 16;
 }
 
 // Output column d of accumulator tile mt, half (0: row g, 1: row g + 8).
@@ -167,278 +197,399 @@ __device__ __forceinline__ int acc_d(int mt, int half, int g) {
     return 16 * mt + g + 8 * half;
 }
 
-template <int KV, int D, typename OutT>
-__global__ void __launch_bounds__(DecodeCfg<KV, D>::kThreads, 1) decode_kernel(AttnParams p) {
-  using C = DecodeCfg<KV, D>;
-  using R = Ring<C::kRowB, C::kRowS, C::kST, C::kNS>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  float* cm = reinterpret_cast<float*>(smem + (size_t)C::kNS * C::kStageB);
-  float* cl = cm + C::kNW * 8;
-  float* co = cl + C::kNW * 8;
-  float* cw = co + C::kNW * 8 * D;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(cw + 8 * kMaxChunks);
-  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * C::kNS);  // [0] abort, [1] last
-  R ring;
-  ring.base = smem;
-  ring.base_s = smem_u32(smem);
-  ring.full0 = smem_u32(bars);
-  ring.empty0 = smem_u32(bars + C::kNS);
-  if (threadIdx.x == 0) flags[0] = flags[1] = 0;
-  init_ring_barriers<C::kNS>(ring.full0, ring.empty0, C::kNW);
+// Byte offset, within a cache, of the HP-head row of logical token j of a
+// sequence, or -1 if its block id is out of range (recorded).
+__device__ __forceinline__ int64_t token_row(const AttnParams& p, const int32_t* bt_row, int j, int hg,
+                                             int row_bytes) {
+  const int lb = p.bs_shift >= 0 ? (j >> p.bs_shift) : (j / p.bs);
+  const int32_t blk = __ldg(bt_row + lb);
+  if (blk < 0 || blk >= p.num_blocks) {
+    atomicOr(p.err, kErrBlockRange);
+    return -1;
+  }
+  return (((int64_t)blk * p.bs + (j - lb * p.bs)) * p.Hkv + (int64_t)hg * p.hp) * (int64_t)row_bytes;
+}
 
+template <int KV, int D, typename OutT>
+__global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(AttnParams p) {
+  using Geo = DecodeGeom<KV, D>;
+  constexpr int RowB = Geo::kRowB, ST = Geo::kST, MT = Geo::kMT, QRowB = Geo::kQRowB;
+  const int HP = p.hp, NS = p.ns, G = p.G;
+  const int tokS = decode_tok_stride<KV, D>(HP);
+  const int stageB = decode_stage_bytes<KV, D>(HP);
+  const int itemB = decode_item_bytes<KV, D>(HP, G);
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* items = smem + (size_t)NS * stageB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(items + 2 * itemB);
+  const uint32_t stage0 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NS;
+  const uint32_t ifull0 = empty0 + 8 * NS, iempty0 = ifull0 + 16;
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * NS + 4);  // [0] abort
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == C::kNW) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, HP);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(ifull0 + 8 * i, 1);
+      mbar_init(iempty0 + 8 * i, HP);
+    }
+    flags[0] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp > HP) return;  // launched with (HP + 1) warps; nothing else to do
+  const int HG = p.Hkv / HP;
+  const int n_items = __ldg(p.ws.dec_off + p.B) * HG;
+
+  if (warp == HP) {
     // ======================= producer warp =======================
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
-    int fill = 0;
-    DecodeItem it;
-    for (int w = blockIdx.x; decode_item(p, w, it); w += gridDim.x) {
-      const int32_t* bt_row = p.bt + (int64_t)it.s * p.bt_stride;
-      for (int j0 = it.k0; j0 < it.k1; j0 += C::kST) {
-        if (flags[0]) break;
-        if (!ring.produce(p, fill, bt_row, it.g, j0, min(C::kST, it.k1 - j0), kbase, vbase, lane)) {
+    const int tok = lane & 15;
+    const bool is_v = lane >= 16;
+    const int copy_b = HP * RowB;
+    int slot = 0, phase = 0, islot = 0, iphase = 0, fills = 0;
+    int w = 0;
+    if (lane == 0) w = atomicAdd(p.ws.work, 1);
+    w = __shfl_sync(0xffffffffu, w, 0);
+    while (w < n_items && !flags[0]) {
+      int wn = 0;
+      if (lane == 0) wn = atomicAdd(p.ws.work, 1);  // the next item, claimed ahead
+      const DecodeDesc d = p.ws.dec_desc[w / HG];
+      const int hg = w - (w / HG) * HG;
+      // ---- publish the item: descriptor and the group's query rows
+      if (!mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) {
+        flags[0] = 1;
+        break;
+      }
+      unsigned char* it = items + islot * itemB;
+      const int q_rows = HP * G;
+      if (lane == 0) {
+        int* meta = reinterpret_cast<int*>(it + q_rows * QRowB);
+        meta[0] = d.s;
+        meta[1] = d.k0;
+        meta[2] = d.k1;
+        meta[3] = d.t;
+        meta[4] = d.nchunks;
+        meta[5] = d.u0 + d.c;
+        meta[6] = hg;
+        meta[7] = d.u0;
+        mbar_arrive_expect_tx(ifull0 + 8 * islot, q_rows * QRowB);
+      }
+      __syncwarp();
+      {
+        const __nv_bfloat16* q0 = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)d.t * p.q_st +
+                                  (int64_t)hg * q_rows * p.q_sh;
+        if (p.q_sh == D) {
+          if (lane == 0) bulk_g2s(smem_u32(it), q0, q_rows * QRowB, ifull0 + 8 * islot);
+        } else {
+          for (int r = lane; r < q_rows; r += 32)
+            bulk_g2s(smem_u32(it + r * QRowB), q0 + (int64_t)r * p.q_sh, QRowB, ifull0 + 8 * islot);
+        }
+      }
+      if (++islot == 2) {
+        islot = 0;
+        iphase ^= 1;
+      }
+      // ---- K/V stages: lanes 0-15 copy K rows, lanes 16-31 V rows
+      const int32_t* bt_row = p.bt + (int64_t)d.s * p.bt_stride;
+      int64_t row_next = d.k0 + tok < d.k1 ? token_row(p, bt_row, d.k0 + tok, hg, RowB) : -1;
+      for (int j0 = d.k0; j0 < d.k1; j0 += ST) {
+        const int64_t row = row_next;
+        const int jn = j0 + ST + tok;
+        row_next = jn < d.k1 ? token_row(p, bt_row, jn, hg, RowB) : -1;  // a stage ahead
+        if (!mbar_wait(empty0 + 8 * slot, phase ^ 1, p.err)) {
           flags[0] = 1;
           break;
         }
-        ++fill;
+        unsigned char* dst = smem + (size_t)slot * stageB + (is_v ? ST * tokS : 0) + tok * tokS;
+        if (row < 0) {  // past the chunk or a bad block id: this token adds nothing
+          uint4* z = reinterpret_cast<uint4*>(dst);
+          for (int i = 0; i < copy_b / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+        }
+        if (__any_sync(0xffffffffu, row < 0)) fence_proxy_async_smem();
+        const unsigned valid = __ballot_sync(0xffffffffu, row >= 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, __popc(valid) * copy_b);
+        __syncwarp();
+        if (row >= 0) bulk_g2s(smem_u32(dst), (is_v ? vbase : kbase) + row, copy_b, full0 + 8 * slot);
+        ++fills;
+        if (++slot == NS) {
+          slot = 0;
+          phase ^= 1;
+        }
       }
-      if (flags[0]) break;
+      w = __shfl_sync(0xffffffffu, wn, 0);
     }
-    ring.drain(p, fill);
+    // ---- no more items: tell the consumers, then let the last copies land
+    if (!flags[0] && mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) {
+      if (lane == 0) {
+        reinterpret_cast<int*>(items + islot * itemB + HP * G * QRowB)[0] = -1;
+        mbar_arrive(ifull0 + 8 * islot);
+      }
+    } else {
+      flags[0] = 1;
+    }
+    for (int f = 0; f < NS && f < fills; ++f) {
+      // stage slots hold the last min(NS, fills) fills; wait for each
+      int sl = slot - 1 - f, ph = phase;
+      if (sl < 0) {
+        sl += NS;
+        ph ^= 1;
+      }
+      if (!mbar_wait(full0 + 8 * sl, ph, p.err)) break;
+    }
     return;
   }
 
-  // ======================= consumer warps =======================
+  // ======================= consumer warp h = warp =======================
+  const int h = warp;
   const int g4 = lane >> 2, t4 = lane & 3;  // fragment row / column-pair index
-  const int nthr = C::kNW * 32;
-  int cons = 0;
-  DecodeItem it;
-  for (int w = blockIdx.x; decode_item(p, w, it); w += gridDim.x) {
+  int slot = 0, phase = 0, islot = 0, iphase = 0;
+  for (;;) {
+    if (!mbar_wait(ifull0 + 8 * islot, iphase, p.err)) {
+      flags[0] = 1;
+      return;
+    }
+    const unsigned char* it = items + islot * itemB;
+    const int* meta = reinterpret_cast<const int*>(it + HP * G * QRowB);
+    const int s = meta[0];
+    if (s < 0) return;  // no more items
+    const int k0 = meta[1], k1 = meta[2], t = meta[3], nchunks = meta[4], u = meta[5], hg = meta[6];
+    const int u0 = meta[7];
+    const int g = hg * HP + h;  // KV head of this warp
     // ---- query fragments (B operand: k = d, n = query head of the group)
-    uint32_t qb[C::kMT][2];
+    uint32_t qb[MT][2];
     {
-      const bool hv = g4 < p.G;
-      const int h = it.g * p.G + (hv ? g4 : 0);
-      const __nv_bfloat16* qrow =
-          static_cast<const __nv_bfloat16*>(p.q) + it.t * p.q_st + (int64_t)h * p.q_sh;
+      const bool hv = g4 < G;
+      const unsigned char* qrow = it + (h * G + (hv ? g4 : 0)) * QRowB;
 #pragma unroll
-      for (int ks = 0; ks < C::kMT; ++ks) {
+      for (int ks = 0; ks < MT; ++ks) {
         if constexpr (KV == 2) {
-          const uint2 v = hv ? *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * t4) : make_uint2(0, 0);
+          const uint2 v = hv ? *reinterpret_cast<const uint2*>(qrow + 2 * (16 * ks + 4 * t4)) : make_uint2(0, 0);
           qb[ks][0] = bf16x2_to_f16x2(v.x);
           qb[ks][1] = bf16x2_to_f16x2(v.y);
         } else {
-          qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4) : 0u;
-          qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4 + 8) : 0u;
+          qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 2 * (16 * ks + 2 * t4)) : 0u;
+          qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 2 * (16 * ks + 2 * t4 + 8)) : 0u;
         }
       }
     }
-    float acc[C::kMT][4];
+    float acc[MT][4];
 #pragma unroll
-    for (int i = 0; i < C::kMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int j0 = it.k0; j0 < it.k1; j0 += C::kST, ++cons) {
-      if (!flags[0] && !ring.wait_full(p, cons)) flags[0] = 1;
-      const int base = j0 + 16 * warp;  // first token of this warp
-      if (base < it.k1 && !flags[0]) {
-        const uint32_t sK = ring.k_rows(cons) + (16 * warp) * C::kRowS;
-        const uint32_t sV = ring.v_rows(cons) + (16 * warp) * C::kRowS;
-        // ---- S = K q^T : rows = 16 tokens, cols = heads
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (KV == 2) {
-          const uint32_t aK = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowS + (lane >> 4) * 16;
+    for (int j0 = k0; j0 < k1; j0 += ST) {
+      if (!mbar_wait(full0 + 8 * slot, phase, p.err)) {
+        flags[0] = 1;
+        return;
+      }
+      const uint32_t sK = stage0 + slot * stageB + h * RowB;
+      const uint32_t sV = sK + ST * tokS;
+      // ---- S = K q^T : rows = 16 tokens, cols = heads
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (KV == 2) {
+        const uint32_t aK = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * tokS + (lane >> 4) * 16;
 #pragma unroll
-          for (int kp = 0; kp < C::kMT / 2; ++kp) {
-            uint32_t w0, w1, w2, w3;
-            ldsm_x4(aK + 32 * kp, w0, w1, w2, w3);
-            uint32_t a[4];
-            e4m3x4_to_f16(w0, a[0], a[2]);
-            e4m3x4_to_f16(w1, a[1], a[3]);
-            mma_f16(s, a, qb[2 * kp][0], qb[2 * kp][1]);
-            e4m3x4_to_f16(w2, a[0], a[2]);
-            e4m3x4_to_f16(w3, a[1], a[3]);
-            mma_f16(s, a, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
-          }
-        } else {
-          const uint32_t aK = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowS + ((lane >> 4) & 1) * 16;
-#pragma unroll
-          for (int ks = 0; ks < C::kMT; ++ks) {
-            uint32_t a[4];
-            ldsm_x4(aK + 32 * ks, a[0], a[1], a[2], a[3]);
-            mma_bf16(s, a, qb[ks][0], qb[ks][1]);
-          }
+        for (int kp = 0; kp < MT / 2; ++kp) {
+          uint32_t w0, w1, w2, w3;
+          ldsm_x4(aK + 32 * kp, w0, w1, w2, w3);
+          uint32_t a[4];
+          e4m3x4_to_f16(w0, a[0], a[2]);
+          e4m3x4_to_f16(w1, a[1], a[3]);
+          mma_f16(sc, a, qb[2 * kp][0], qb[2 * kp][1]);
+          e4m3x4_to_f16(w2, a[0], a[2]);
+          e4m3x4_to_f16(w3, a[1], a[3]);
+          mma_f16(sc, a, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
         }
-        // ---- online softmax (base 2) per head column
-        const bool v0 = base + g4 < it.k1, v1 = base + g4 + 8 < it.k1;
-        const float x0 = v0 ? s[0] * p.qk_scale_log2 : -INFINITY;
-        const float x1 = v0 ? s[1] * p.qk_scale_log2 : -INFINITY;
-        const float x2 = v1 ? s[2] * p.qk_scale_log2 : -INFINITY;
-        const float x3 = v1 ? s[3] * p.qk_scale_log2 : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-        mx0 = warp_max_xor(mx0, 4); mx0 = warp_max_xor(mx0, 8); mx0 = warp_max_xor(mx0, 16);
-        mx1 = warp_max_xor(mx1, 4); mx1 = warp_max_xor(mx1, 8); mx1 = warp_max_xor(mx1, 16);
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
-        const float p0 = exp2f(x0 - ms0), p1 = exp2f(x1 - ms1);
-        const float p2 = exp2f(x2 - ms0), p3 = exp2f(x3 - ms1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
+      } else {
+        const uint32_t aK = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * tokS + ((lane >> 4) & 1) * 16;
 #pragma unroll
-        for (int i = 0; i < C::kMT; ++i) {
-          acc[i][0] *= al0;
-          acc[i][1] *= al1;
-          acc[i][2] *= al0;
-          acc[i][3] *= al1;
-        }
-        // ---- O^T += V^T P : rows = d, cols = heads, k = tokens
-        if constexpr (KV == 2) {
-          const uint32_t b0 = movm_t(pack_f16(p0, p1)), b1 = movm_t(pack_f16(p2, p3));
-          const uint32_t aV = sV + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowS + (lane >> 4) * 16;
-#pragma unroll
-          for (int cp = 0; cp < C::kMT / 2; ++cp) {
-            uint32_t w0, w1, w2, w3;
-            ldsm_x4(aV + 32 * cp, w0, w1, w2, w3);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t wt = hh ? w2 : w0, wb = hh ? w3 : w1;
-              uint32_t x0t, x1t, x0b, x1b;
-              e4m3x4_to_f16(wt, x0t, x1t);
-              e4m3x4_to_f16(wb, x0b, x1b);
-              const uint32_t a[4] = {movm_t(x0t), movm_t(x1t), movm_t(x0b), movm_t(x1b)};
-              mma_f16(acc[2 * cp + hh], a, b0, b1);
-            }
-          }
-        } else {
-          uint32_t hi0, lo0, hi1, lo1;
-          split_bf16(p0, p1, hi0, lo0);
-          split_bf16(p2, p3, hi1, lo1);
-          const uint32_t bh0 = movm_t(hi0), bh1 = movm_t(hi1), bl0 = movm_t(lo0), bl1 = movm_t(lo1);
-          const uint32_t aV = sV + ((lane & 7) + ((lane >> 4) & 1) * 8) * C::kRowS + ((lane >> 3) & 1) * 16;
-#pragma unroll
-          for (int mt = 0; mt < C::kMT; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_t(aV + 32 * mt, a[0], a[1], a[2], a[3]);
-            mma_bf16(acc[mt], a, bh0, bh1);
-            mma_bf16(acc[mt], a, bl0, bl1);
-          }
+        for (int ks = 0; ks < MT; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(aK + 32 * ks, a[0], a[1], a[2], a[3]);
+          mma_bf16(sc, a, qb[ks][0], qb[ks][1]);
         }
       }
-      ring.release(cons, lane);
+      // ---- online softmax (base 2) per head column
+      const bool v0 = j0 + g4 < k1, v1 = j0 + g4 + 8 < k1;
+      const float x0 = v0 ? sc[0] * p.qk_scale_log2 : -INFINITY;
+      const float x1 = v0 ? sc[1] * p.qk_scale_log2 : -INFINITY;
+      const float x2 = v1 ? sc[2] * p.qk_scale_log2 : -INFINITY;
+      const float x3 = v1 ? sc[3] * p.qk_scale_log2 : -INFINITY;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      mx0 = warp_max_xor(mx0, 4); mx0 = warp_max_xor(mx0, 8); mx0 = warp_max_xor(mx0, 16);
+      mx1 = warp_max_xor(mx1, 4); mx1 = warp_max_xor(mx1, 8); mx1 = warp_max_xor(mx1, 16);
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
+      const float p0 = exp2f(x0 - ms0), p1 = exp2f(x1 - ms1);
+      const float p2 = exp2f(x2 - ms0), p3 = exp2f(x3 - ms1);
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
+      // ---- O^T += V^T P : rows = d, cols = heads, k = tokens
+      if constexpr (KV == 2) {
+        const uint32_t b0 = movm_t(pack_f16(p0, p1)), b1 = movm_t(pack_f16(p2, p3));
+        const uint32_t aV = sV + ((lane & 7) + ((lane >> 3) & 1) * 8) * tokS + (lane >> 4) * 16;
+#pragma unroll
+        for (int cp = 0; cp < MT / 2; ++cp) {
+          uint32_t w0, w1, w2, w3;
+          ldsm_x4(aV + 32 * cp, w0, w1, w2, w3);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t x0t, x1t, x0b, x1b;
+            e4m3x4_to_f16(hh ? w2 : w0, x0t, x1t);
+            e4m3x4_to_f16(hh ? w3 : w1, x0b, x1b);
+            const uint32_t a[4] = {movm_t(x0t), movm_t(x1t), movm_t(x0b), movm_t(x1b)};
+            mma_f16(acc[2 * cp + hh], a, b0, b1);
+          }
+        }
+      } else {
+        uint32_t hi0, lo0, hi1, lo1;
+        split_bf16(p0, p1, hi0, lo0);
+        split_bf16(p2, p3, hi1, lo1);
+        const uint32_t bh0 = movm_t(hi0), bh1 = movm_t(hi1), bl0 = movm_t(lo0), bl1 = movm_t(lo1);
+        const uint32_t aV = sV + ((lane & 7) + ((lane >> 4) & 1) * 8) * tokS + ((lane >> 3) & 1) * 16;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(aV + 32 * mt, a[0], a[1], a[2], a[3]);
+          mma_bf16(acc[mt], a, bh0, bh1);
+          mma_bf16(acc[mt], a, bl0, bl1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      if (++slot == NS) {
+        slot = 0;
+        phase ^= 1;
+      }
     }
 
-    // ---- combine the four warps (fixed order) -------------------------
+    // ---- epilogue of this warp's head
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    if (lane < 4) {
-      cm[warp * 8 + 2 * lane] = m0;
-      cm[warp * 8 + 2 * lane + 1] = m1;
-      cl[warp * 8 + 2 * lane] = l0;
-      cl[warp * 8 + 2 * lane + 1] = l1;
-    }
-    named_sync(1, nthr);
-    {
-      const int c0 = 2 * t4, c1 = c0 + 1;
-      float M0 = -INFINITY, M1 = -INFINITY;
+    const int c0 = 2 * t4, c1 = c0 + 1;  // this thread's head columns
+    const float r0 = p.v_scale / l0, r1 = p.v_scale / l1;
+    const int hq0 = g * G;
+    if (nchunks == 1) {
 #pragma unroll
-      for (int v = 0; v < C::kNW; ++v) {
-        M0 = fmaxf(M0, cm[v * 8 + c0]);
-        M1 = fmaxf(M1, cm[v * 8 + c1]);
-      }
-      const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-      const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
-      float* cow = co + warp * 8 * D;
-#pragma unroll
-      for (int mt = 0; mt < C::kMT; ++mt) {
+      for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int d = acc_d<KV>(mt, half, g4);
-          cow[c0 * D + d] = acc[mt][2 * half] * f0;
-          cow[c1 * D + d] = acc[mt][2 * half + 1] * f1;
+          const int dd = acc_d<KV>(mt, half, g4);
+          if (c0 < G) store1(static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + c0) * p.o_sh + dd,
+                             acc[mt][2 * half] * r0);
+          if (c1 < G) store1(static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + c1) * p.o_sh + dd,
+                             acc[mt][2 * half + 1] * r1);
         }
       }
-    }
-    named_sync(1, nthr);
-    const int hq0 = it.g * p.G;
-    const bool single = it.nchunks == 1;
-    for (int e = threadIdx.x; e < p.G * D; e += nthr) {
-      const int col = e / D, d = e - col * D;
-      float M = -INFINITY;
+    } else {
+      float* po = p.ws.part_o + (int64_t)u * p.Hq * D;
 #pragma unroll
-      for (int v = 0; v < C::kNW; ++v) M = fmaxf(M, cm[v * 8 + col]);
-      float L = 0.f, o = 0.f;
+      for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-      for (int v = 0; v < C::kNW; ++v) {
-        const float mv = cm[v * 8 + col];
-        L += (mv == -INFINITY ? 0.f : exp2f(mv - M)) * cl[v * 8 + col];
-        o += co[(v * 8 + col) * D + d];
-      }
-      const float val = o / L * p.v_scale;
-      const int h = hq0 + col;
-      if (single) {
-        store1(static_cast<OutT*>(p.out) + it.t * p.o_st + (int64_t)h * p.o_sh + d, val);
-      } else {
-        p.ws.part_o[((int64_t)it.u * p.Hq + h) * D + d] = val;
-        if (d == 0) p.ws.part_lse[(int64_t)it.u * p.Hq + h] = M + log2f(L);
-      }
-    }
-    if (!single) {
-      // ---- last chunk of (s, g) to finish merges all of them -----------
-      __threadfence();
-      named_sync(1, nthr);
-      if (threadIdx.x == 0) {
-        const int done = atomicAdd(p.ws.counters + it.s * p.Hkv + it.g, 1);
-        flags[1] = done == it.nchunks - 1;
-      }
-      named_sync(1, nthr);
-      if (flags[1]) {
-        __threadfence();
-        const int u0 = __ldg(p.ws.dec_off + it.s);
-        // chunk weights 2^(lse_c - max) per head column
-        for (int e = threadIdx.x; e < p.G * it.nchunks; e += nthr) {
-          const int col = e / it.nchunks, c = e - col * it.nchunks;
-          cw[col * kMaxChunks + c] = __ldcg(p.ws.part_lse + (int64_t)(u0 + c) * p.Hq + hq0 + col);
+        for (int half = 0; half < 2; ++half) {
+          const int dd = acc_d<KV>(mt, half, g4);
+          if (c0 < G) po[(int64_t)(hq0 + c0) * D + dd] = acc[mt][2 * half] * r0;
+          if (c1 < G) po[(int64_t)(hq0 + c1) * D + dd] = acc[mt][2 * half + 1] * r1;
         }
-        named_sync(1, nthr);
-        for (int e = threadIdx.x; e < p.G * D; e += nthr) {
-          const int col = e / D, d = e - col * D;
+      }
+      if (g4 == 0) {
+        if (c0 < G) p.ws.part_lse[(int64_t)u * p.Hq + hq0 + c0] = m0 + log2f(l0);
+        if (c1 < G) p.ws.part_lse[(int64_t)u * p.Hq + hq0 + c1] = m1 + log2f(l1);
+      }
+      // ---- the warp that finishes the last chunk of (s, g) merges them
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();  // cumulative over the warp's writes ordered by __syncwarp
+        last = atomicAdd(p.ws.counters + s * p.Hkv + g, 1) == nchunks - 1;
+        if (last) __threadfence();
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        for (int col = 0; col < G; ++col) {
+          const float* lse = p.ws.part_lse + (int64_t)u0 * p.Hq + hq0 + col;
           float M = -INFINITY;
-          for (int c = 0; c < it.nchunks; ++c) M = fmaxf(M, cw[col * kMaxChunks + c]);
-          float L = 0.f, o = 0.f;
-          for (int c = 0; c < it.nchunks; ++c) {
-            const float wgt = exp2f(cw[col * kMaxChunks + c] - M);
+          for (int c = lane; c < nchunks; c += 32) M = fmaxf(M, __ldcg(lse + (int64_t)c * p.Hq));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+          float L = 0.f, o[D / 32];
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) o[k] = 0.f;
+          for (int c = 0; c < nchunks; ++c) {
+            const float wgt = exp2f(__ldcg(lse + (int64_t)c * p.Hq) - M);
             L += wgt;
-            o += wgt * __ldcg(p.ws.part_o + ((int64_t)(u0 + c) * p.Hq + hq0 + col) * D + d);
+            const float* src = p.ws.part_o + ((int64_t)(u0 + c) * p.Hq + hq0 + col) * D;
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) o[k] += wgt * __ldcg(src + lane + 32 * k);
           }
-          store1(static_cast<OutT*>(p.out) + it.t * p.o_st + (int64_t)(hq0 + col) * p.o_sh + d, o / L);
+          OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + col) * p.o_sh;
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) store1(dst + lane + 32 * k, o[k] / L);
         }
       }
     }
-    named_sync(1, nthr);  // the combine area is reused by the next item
+    __syncwarp();
+    if (lane == 0) mbar_arrive(iempty0 + 8 * islot);
+    if (++islot == 2) {
+      islot = 0;
+      iphase ^= 1;
+    }
   }
 }
 
 // ---------------------------------------------------------------- launch
+// Decode geometry for a head count: HP KV heads per item (a divisor of Hkv,
+// at most 8) and as many stages as fit in shared memory.
+template <int KV, int D>
+static bool decode_geometry(int Hkv, int G, int& hp, int& ns) {
+  const size_t budget = 227 * 1024;
+  for (hp = 8; hp >= 1; --hp) {
+    if (Hkv % hp) continue;
+    for (ns = 8; ns >= 3; --ns)
+      if (decode_smem<KV, D>(hp, ns, G) <= budget) return true;
+  }
+  return false;
+}
+
 template <int KV, int D, typename OutT>
-static cudaError_t launch_decode_t(const AttnParams& p, int64_t max_items, int num_sms, cudaStream_t st) {
-  using C = DecodeCfg<KV, D>;
+static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms, cudaStream_t st) {
+  using Geo = DecodeGeom<KV, D>;
+  int hp = 1, ns = 3;
+  if (!decode_geometry<KV, D>(p.Hkv, p.G, hp, ns)) return cudaErrorInvalidConfiguration;
+  p.hp = hp;
+  p.ns = ns;
+  const size_t smem = decode_smem<KV, D>(hp, ns, p.G);
   auto kern = decode_kernel<KV, D, OutT>;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern), C::kSmem);
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024);
   if (e != cudaSuccess) return e;
+  const int threads = (hp + 1) * 32;
   int occ = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads, C::kSmem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
   if (occ < 1) occ = 1;
   int64_t grid = (int64_t)num_sms * occ;
-  if (grid > max_items) grid = max_items;
+  const int64_t items = (max_items + hp - 1) / hp;  // max_items counts (unit, KV head) pairs
+  if (grid > items) grid = items;
   if (grid < 1) return cudaSuccess;
-  kern<<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(p);
+  (void)Geo::kThreads;
+  kern<<<(unsigned)grid, threads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -35,12 +35,36 @@ cudaError_t launch_append(const AppendParams& p, int src_kind, bool fp8, bool sl
 
 // ---------------------------------------------------------------- attention
 // Device workspace of one attention call (all offsets 256-byte aligned).
+// One decode unit: a logical chunk of one sequence (all KV heads share it).
+struct DecodeDesc {
+  int32_t s;        // sequence
+  int32_t k0, k1;   // keys k0 .. k1-1
+  int32_t t;        // packed row of the sequence's query token
+  int32_t nchunks;  // chunks of the sequence
+  int32_t u0;       // unit index of the sequence's first chunk
+  int32_t c;        // chunk index
+  int32_t pad;
+};
+
+// One prefill tile: 64 consecutive (token, head-of-group) rows of a sequence.
+struct PrefillDesc {
+  int32_t s;
+  int32_t t0;       // packed row of the sequence's first query token
+  int32_t q_s, n;   // query rows and keys of the sequence
+  int32_t r0, r1;   // rows r0 .. r1-1 of q_s * G
+  int32_t kv_end;   // keys 0 .. kv_end-1 are visible to some row
+  int32_t pad;
+};
+
 struct Workspace {
-  int32_t* dec_off;    // [B+1] prefix sums of decode chunk units
-  int32_t* pf_off;     // [B+1] prefix sums of prefill row tiles
-  int32_t* counters;   // [B * Hkv] chunks finished per (sequence, KV head)
-  float* part_o;       // [B * kMaxChunks, Hq, D] chunk outputs (normalised)
-  float* part_lse;     // [B * kMaxChunks, Hq] chunk log2-sum-exp2
+  int32_t* dec_off;      // [B+1] prefix sums of decode chunk units
+  int32_t* pf_off;       // [B+1] prefix sums of prefill row tiles
+  int32_t* counters;     // [B * Hkv] chunks finished per (sequence, KV head)
+  int32_t* work;         // [1] next decode item to hand out
+  DecodeDesc* dec_desc;  // [B * max_chunks] decode units in order
+  PrefillDesc* pf_desc;  // [max prefill tiles] prefill tiles in order
+  float* part_o;         // [B * max_chunks, Hq, D] chunk outputs (normalised)
+  float* part_lse;       // [B * max_chunks, Hq] chunk log2-sum-exp2
 };
 
 struct AttnParams {
@@ -67,12 +91,16 @@ struct AttnParams {
   float qk_scale_log2;  // scale * k_scale * log2(e)
   float v_scale;        // applied to the output (e4m3 caches), else 1
   int32_t decode_max_g;  // sequences with q_s == 1 and G <= this take the decode path
+  int32_t hp;            // decode: KV heads per work item (consumer warps), divides Hkv, <= 8
+  int32_t ns;            // decode: stages in the staging ring
   Workspace ws;
   unsigned int* err;
 };
 
 // Launchers.  out_kind: 0 = f32, 1 = bf16.  kv: 0 = f32, 1 = bf16, 2 = e4m3.
-size_t attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t D);
+// Prefill tiles of a call are at most ceil(T * G / 64) + B; decode chunks at
+// most B * max_chunks_for(max_blocks * block_size).
+size_t attention_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_ctx);
 
 // Raises a kernel's dynamic shared memory limit once per device.
 cudaError_t set_smem_attr(const void* kernel, size_t bytes);

@@ -30,8 +30,7 @@ struct Ring {
                                           int lane) const {
     const int slot = fill % kNS;
     const uint32_t full = full0 + 8 * slot, empty = empty0 + 8 * slot;
-    if (!mbar_wait(empty, ((fill / kNS) & 1) ^ 1, p.err)) return false;
-    const uint32_t sK = base_s + slot * kStageB, sV = sK + kST * kRowS;
+    // row addresses first: the block-table loads overlap the wait below
     int64_t src[kST / 32];  // byte offset of the row in the cache, -1 = none
     uint32_t bytes = 0;
 #pragma unroll
@@ -50,7 +49,14 @@ struct Ring {
           atomicOr(p.err, kErrBlockRange);
         }
       }
+    }
+    if (!mbar_wait(empty, ((fill / kNS) & 1) ^ 1, p.err)) return false;
+    const uint32_t sK = base_s + slot * kStageB, sV = sK + kST * kRowS;
+    bool zeroed = false;
+#pragma unroll
+    for (int r = 0; r < kST / 32; ++r) {
       if (src[r] < 0) {
+        const int jj = lane + 32 * r;
         uint4* zk = reinterpret_cast<uint4*>(base + slot * kStageB + jj * kRowS);
         uint4* zv = reinterpret_cast<uint4*>(base + slot * kStageB + (kST + jj) * kRowS);
 #pragma unroll
@@ -58,9 +64,10 @@ struct Ring {
           zk[i] = make_uint4(0, 0, 0, 0);
           zv[i] = make_uint4(0, 0, 0, 0);
         }
+        zeroed = true;
       }
     }
-    fence_proxy_async_smem();
+    if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
     __syncwarp();

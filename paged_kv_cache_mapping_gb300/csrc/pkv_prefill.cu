@@ -43,19 +43,17 @@ struct PrefillItem {
   int64_t t0;                // packed index of the sequence's first query token
 };
 
-__device__ __forceinline__ bool prefill_item(const AttnParams& p, int w, PrefillItem& it) {
-  const int units = __ldg(p.ws.pf_off + p.B);
-  if (w >= units * p.Hkv) return false;
-  const int u = w / p.Hkv;
-  it.g = w - u * p.Hkv;
-  it.s = upper_index(p.ws.pf_off, p.B, u);
-  const int qt = u - __ldg(p.ws.pf_off + it.s);
-  it.t0 = __ldg(p.cu_q + it.s);
-  it.q_s = __ldg(p.cu_q + it.s + 1) - static_cast<int>(it.t0);
-  it.n = __ldg(p.seq_lens + it.s);
-  it.r0 = qt * kPrefillRows;
-  it.r1 = min(it.r0 + kPrefillRows, it.q_s * p.G);
-  it.kv_end = it.n - it.q_s + (it.r1 - 1) / p.G + 1;
+__device__ __forceinline__ bool prefill_item(const AttnParams& p, int n_items, int w, PrefillItem& it) {
+  if (w >= n_items) return false;
+  const PrefillDesc e = p.ws.pf_desc[w / p.Hkv];
+  it.g = w % p.Hkv;
+  it.s = e.s;
+  it.t0 = e.t0;
+  it.q_s = e.q_s;
+  it.n = e.n;
+  it.r0 = e.r0;
+  it.r1 = e.r1;
+  it.kv_end = e.kv_end;
   return true;
 }
 
@@ -75,13 +73,14 @@ __global__ void __launch_bounds__(PrefillCfg<KV, D>::kThreads, 2) prefill_kernel
   init_ring_barriers<C::kNS>(ring.full0, ring.empty0, C::kNW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = __ldg(p.ws.pf_off + p.B) * p.Hkv;
   if (warp == C::kNW) {
     // ======================= producer warp =======================
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
     int fill = 0;
     PrefillItem it;
-    for (int w = blockIdx.x; prefill_item(p, w, it); w += gridDim.x) {
+    for (int w = blockIdx.x; prefill_item(p, n_items, w, it); w += gridDim.x) {
       const int32_t* bt_row = p.bt + (int64_t)it.s * p.bt_stride;
       for (int j0 = 0; j0 < it.kv_end; j0 += C::kST) {
         if (flags[0]) break;
@@ -101,7 +100,7 @@ __global__ void __launch_bounds__(PrefillCfg<KV, D>::kThreads, 2) prefill_kernel
   const int g4 = lane >> 2, t4 = lane & 3;
   int cons = 0;
   PrefillItem it;
-  for (int w = blockIdx.x; prefill_item(p, w, it); w += gridDim.x) {
+  for (int w = blockIdx.x; prefill_item(p, n_items, w, it); w += gridDim.x) {
     // rows of this thread: A = 16*warp + g4, B = A + 8 (tile-relative)
     const int rA = it.r0 + 16 * warp + g4, rB = rA + 8;
     const bool vA = rA < it.r1, vB = rB < it.r1;

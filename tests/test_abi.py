@@ -115,8 +115,14 @@ def test_workspace_size_is_host_only(lib):
     n = ctypes.c_size_t(0)
     assert lib.pkv_attention_workspace_size(ctypes.byref(a["q"]), ctypes.byref(a["bt"]),
                                             ctypes.byref(a["kc"]), ctypes.byref(n)) == 0
-    # two prefix arrays, counters, 32 chunk outputs and log-sum-exps per sequence
-    assert n.value >= 64 * 32 * 32 * (128 + 1) * 4
+    # block tables of 8 x 16 tokens: one split-KV chunk per sequence at most,
+    # so at least one chunk output and log-sum-exp per (sequence, head)
+    assert n.value >= 64 * 1 * 32 * (128 + 1) * 4
+    c = good(B=64, mb=4096)  # 65536-token tables: 128 chunks of 512 tokens
+    k = ctypes.c_size_t(0)
+    lib.pkv_attention_workspace_size(ctypes.byref(c["q"]), ctypes.byref(c["bt"]), ctypes.byref(c["kc"]),
+                                     ctypes.byref(k))
+    assert k.value >= 64 * 128 * 32 * (128 + 1) * 4
     b = good(B=128)
     m = ctypes.c_size_t(0)
     lib.pkv_attention_workspace_size(ctypes.byref(b["q"]), ctypes.byref(b["bt"]), ctypes.byref(b["kc"]),
