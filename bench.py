@@ -229,6 +229,7 @@ def run_ours(args, rank, world):
                      "traffic": rec["dram_bytes_per_launch"] if rec else None,
                      "algorithmic_bytes": nb["attention"], "avg_launch_us": round(attn_avg_ms * 1e3, 2)},
         "e2e": e2e,
+        # slot mapping, append, plan, decode (+ prefill)
         "gpu_launches": (5 if max_q > 1 else 4) * args.steps,
         "clocks": clk.summary(),
     }

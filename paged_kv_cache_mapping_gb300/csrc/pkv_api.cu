@@ -225,7 +225,7 @@ static int64_t max_prefill_tiles(int64_t B, int64_t T, int64_t G) {
 }
 
 struct WsLayout {
-  size_t dec_off, pf_off, counters, work, dec_desc, pf_desc, part_o, part_lse, total;
+  size_t dec_off, pf_off, work, merge_list, done, dec_desc, pf_desc, part_o, part_lse, total;
 };
 
 static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_ctx) {
@@ -235,8 +235,9 @@ static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t
   size_t n = 0;
   L.dec_off = n;  n += align_up(sizeof(int32_t) * (B + 1), 256);
   L.pf_off = n;   n += align_up(sizeof(int32_t) * (B + 1), 256);
-  L.counters = n; n += align_up(sizeof(int32_t) * B * Hkv, 256);
-  L.work = n;     n += 256;
+  L.work = n;     n += 256;  // work counter, merge count
+  L.merge_list = n; n += align_up(sizeof(int32_t) * B, 256);
+  L.done = n;     n += align_up(sizeof(int32_t) * B * Hkv, 256);
   L.dec_desc = n; n += align_up(sizeof(DecodeDesc) * units, 256);
   L.pf_desc = n;  n += align_up(sizeof(PrefillDesc) * max_prefill_tiles(B, T, G), 256);
   L.part_o = n;   n += align_up(sizeof(float) * units * Hq * D, 256);
@@ -414,6 +415,8 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
   PKV_TRY(need(out->dtype == PKV_F32 || out->dtype == PKV_BF16, "out must be f32 or bf16"));
   PKV_TRY(need(block_tables->shape[1] * bs <= INT32_MAX, "max_blocks * block_size beyond int32"));
   PKV_TRY(need(T <= INT32_MAX, "T beyond int32"));
+  if (NB * bs > INT32_MAX)
+    return fail(PKV_ERR_UNSUPPORTED, "num_blocks * block_size beyond int32 (slots are 32-bit in attention)");
   int kv;
   if (q->dtype == PKV_F32 && k_cache->dtype == PKV_F32)
     kv = 0;
@@ -494,8 +497,10 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
     char* w = static_cast<char*>(workspace);
     p.ws.dec_off = reinterpret_cast<int32_t*>(w + L.dec_off);
     p.ws.pf_off = reinterpret_cast<int32_t*>(w + L.pf_off);
-    p.ws.counters = reinterpret_cast<int32_t*>(w + L.counters);
     p.ws.work = reinterpret_cast<int32_t*>(w + L.work);
+    p.ws.n_merge = p.ws.work + 1;
+    p.ws.merge_list = reinterpret_cast<int32_t*>(w + L.merge_list);
+    p.ws.done = reinterpret_cast<int32_t*>(w + L.done);
     p.ws.dec_desc = reinterpret_cast<pkv::DecodeDesc*>(w + L.dec_desc);
     p.ws.pf_desc = reinterpret_cast<pkv::PrefillDesc*>(w + L.pf_desc);
     p.ws.part_o = reinterpret_cast<float*>(w + L.part_o);
@@ -512,7 +517,9 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
   }
   if (G <= p.decode_max_g) {
     const int64_t dec_seqs = std::min<int64_t>(B, T);
-    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * pkv::max_chunks_for(max_ctx) * Hkv, sms, st);
+    // right after the plan the decode kernel may overlap its start with the
+    // plan's end (it waits for the plan's lists on the device)
+    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * pkv::max_chunks_for(max_ctx) * Hkv, sms, st, !prefill);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return finish(st, "pkv_attention");

@@ -26,17 +26,19 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 
 // Logical tiling.  Every tile and split boundary is a logical token position
 // so that the result does not depend on block_size or page placement.
-constexpr int kChunkBase = 256;       // smallest split-KV chunk (tokens)
+constexpr int kChunkBase = 128;       // smallest split-KV chunk (tokens)
 constexpr int kMaxChunks = 128;       // a sequence is split into at most this many chunks
 constexpr int kPrefillRows = 64;      // (query token, head) rows per prefill tile
 
-// Chunk length of a decoding sequence of n keys: the smallest 256 * 2^k
-// that splits it into at most kMaxChunks chunks.  Depends on n only.
-__host__ __device__ inline int chunk_tokens(int n) {
-  int64_t c = kChunkBase;
-  while (((int64_t)n + c - 1) / c > kMaxChunks) c <<= 1;
-  return static_cast<int>(c);
+// Chunk length of a decoding sequence of n keys: the smallest 128 * 2^k
+// that splits it into at most kMaxChunks chunks, as a shift (chunk =
+// 1 << shift).  Depends on n only.
+__host__ __device__ inline int chunk_shift(int n) {
+  int k = 7;  // 128 tokens
+  while ((((unsigned)n + (1u << k) - 1u) >> k) > (unsigned)kMaxChunks) ++k;
+  return k;
 }
+__host__ __device__ inline int chunk_tokens(int n) { return 1 << chunk_shift(n); }
 
 // Chunks of the longest sequence a block table of max_ctx tokens can hold.
 __host__ __device__ inline int max_chunks_for(int64_t max_ctx) {
@@ -109,6 +111,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream runs;
+// grid_dep_wait() blocks until that kernel has completed and its writes are
+// visible.  launch_dependents() lets the next kernel start early.  Both are
+// no-ops for a kernel launched normally.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Named barrier over the first `threads` threads (consumer warps only).
 __device__ __forceinline__ void named_sync(int id, int threads) {

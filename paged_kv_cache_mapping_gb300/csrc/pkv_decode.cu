@@ -9,21 +9,21 @@
 //
 // Design (GB300):
 //   * A work item is (sequence, logical chunk, group of HP KV heads).  The
-//     chunk length depends only on N_s (256 * 2^k tokens, at most 128
+//     chunk length depends only on N_s (128 * 2^k tokens, at most 128
 //     chunks), so results depend neither on the batch nor on the page layout
 //     ("How Easy Is It to Start Serving LLMs?", "3. Load balancing": long
 //     requests are split into chunks and a merge step stitches them).  The
-//     plan kernel lists the chunks once per call; persistent CTAs (one per
-//     SM) claim items from a global counter, so every SM stays busy to the
-//     end.
+//     plan kernel lists the chunks once per call, every full chunk before
+//     the ragged last ones; persistent CTAs (one per SM) claim items from a
+//     global counter, so every SM stays busy to the end.
 //   * One producer warp per CTA stages the chunk 16 logical tokens at a time:
 //     a token's K row for all HP heads of the group is HP * D contiguous
 //     elements of the cache (2 KB at D = 128, bf16, HP = 8), fetched with one
 //     1-D bulk copy (TMA) that completes on the stage's mbarrier; V likewise.
 //     Whole-token copies keep the number of TMA requests low, which is what
-//     limits a TMA gather of small rows.  Block ids are fetched a stage
-//     ahead; the item's descriptor and query rows go through a two-slot item
-//     ring.  Every page is read once for all Hq/Hkv query heads.
+//     limits a TMA gather of small rows.  Block ids are fetched a group of
+//     16 stages ahead; the item's descriptor and query rows go through a
+//     two-slot item ring.  Every page is read once for all Hq/Hkv query heads.
 //   * Consumer warp h owns KV head h of the group for the whole chunk: S =
 //     K q^T and O^T += V^T P run on the tensor cores (mma.sync m16n8k16)
 //     with the 16 keys of a stage as M and the head's G query heads as N, so
@@ -32,133 +32,155 @@
 //     (two MMAs; about 16 significant bits); with an e4m3 cache K and V are
 //     converted exactly to f16 and P is f16.
 //   * A sequence of one chunk writes its output directly.  Otherwise each
-//     chunk writes its normalised output and log2-sum-exp2 to the workspace,
-//     and the warp that finishes the last chunk of a (sequence, KV head)
-//     merges them in chunk order (no separate merge launch, no CTA-wide
-//     synchronisation).
+//     chunk writes its normalised output and log2-sum-exp2 to the workspace;
+//     once all the decode items are handed out, the same queue hands out one
+//     merge item per (split sequence, head group), which waits until the
+//     producers of the other CTAs report the sequence's chunks finished and
+//     combines them in chunk order -- the CTAs that run out of chunks merge
+//     while the others finish, with no second kernel launch.
+#include <algorithm>
+
 #include "pkv_pipeline.cuh"
 
 namespace pkv {
 
 // ---------------------------------------------------------------- plan
-// One block: per-sequence work counts, their exclusive prefix sums, the
-// descriptor lists of decode chunks and prefill tiles, and the merge
-// counters reset.  Reads device lengths; no host round trip.
+// Block-wide exclusive scan of K counts per thread (warp shuffles, then one
+// warp over the warp totals).  off[] = the thread's offsets, totals[] = the
+// block totals.
+template <int K>
+__device__ __forceinline__ void block_scan(const int (&v)[K], int (&off)[K], int (&totals)[K]) {
+  __shared__ int wsum[32][K];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) x[k] = v[k];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
+  }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < K; ++k) wsum[warp][k] = x[k];
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      int y = lane < nw ? wsum[lane][k] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int z = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += z;
+      }
+      if (lane < nw) wsum[lane][k] = y;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    off[k] = x[k] - v[k] + (warp > 0 ? wsum[warp - 1][k] : 0);
+    totals[k] = wsum[nw - 1][k];
+  }
+}
+
+// Work counts of sequence s: decode chunks (all, full, ragged last) or
+// prefill tiles.  Inconsistent lengths give no work (and are recorded).
+struct SeqCounts {
+  int dec, full, tail, pf;
+};
+
+__device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool record) {
+  SeqCounts c{0, 0, 0, 0};
+  const int c0 = __ldg(p.cu_q + s), c1 = __ldg(p.cu_q + s + 1);
+  const int q_s = c1 - c0;
+  const int n = __ldg(p.seq_lens + s);
+  if (q_s == 0) return c;
+  if (q_s < 0 || q_s > n || (int64_t)n > (int64_t)p.max_blocks * p.bs || c0 < 0 || c1 > p.T) {
+    if (record) atomicOr(p.err, kErrLengths);
+    return c;
+  }
+  if (q_s == 1 && p.G <= p.decode_max_g) {
+    const int k = chunk_shift(n);
+    c.dec = (int)(((unsigned)n + (1u << k) - 1u) >> k);
+    c.full = n >> k;
+    c.tail = c.dec - c.full;
+  } else {
+    c.pf = (int)(((int64_t)q_s * p.G + kPrefillRows - 1) / kPrefillRows);
+  }
+  return c;
+}
+
+// One block: per-sequence work counts and their prefix sums, the decode
+// work list (every full chunk first, then the ragged last chunks, so that
+// the small pieces come last), the list of split sequences, the prefill
+// tile list, and the per-call counters reset.  Reads device lengths; no
+// host round trip.
 __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
-  __shared__ int warp_d[32], warp_p[32];
+  launch_dependents();  // the decode kernel may start its set-up now
   const int tid = threadIdx.x, nth = blockDim.x;
   const int B = p.B;
   const int per = (B + nth - 1) / nth;
   const int s0 = min(tid * per, B), s1 = min(s0 + per, B);
-  auto counts = [&](int s, int& dec, int& pf) {
-    const int c0 = __ldg(p.cu_q + s), c1 = __ldg(p.cu_q + s + 1);
-    const int q_s = c1 - c0;
-    const int n = __ldg(p.seq_lens + s);
-    dec = pf = 0;
-    if (q_s == 0) return;
-    if (q_s < 0 || q_s > n || (int64_t)n > (int64_t)p.max_blocks * p.bs || c0 < 0 || c1 > p.T) {
-      atomicOr(p.err, kErrLengths);
-      return;
-    }
-    if (q_s == 1 && p.G <= p.decode_max_g) {
-      const int c = chunk_tokens(n);
-      dec = (n + c - 1) / c;
-    } else {
-      pf = (int)(((int64_t)q_s * p.G + kPrefillRows - 1) / kPrefillRows);
-    }
-  };
-  int dsum = 0, psum = 0;
+  SeqCounts first{0, 0, 0, 0};  // the thread's first sequence, kept for the second pass
+  int sum[5] = {0, 0, 0, 0, 0};
   for (int s = s0; s < s1; ++s) {
-    int d, f;
-    counts(s, d, f);
-    dsum += d;
-    psum += f;
+    const SeqCounts c = seq_counts(p, s, true);
+    if (s == s0) first = c;
+    sum[0] += c.dec;
+    sum[1] += c.full;
+    sum[2] += c.tail;
+    sum[3] += c.pf;
+    sum[4] += c.dec > 1;
   }
-  // block-wide exclusive scan of (dsum, psum)
-  const int lane = tid & 31, warp = tid >> 5;
-  int xd = dsum, xp = psum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int yd = __shfl_up_sync(0xffffffffu, xd, o), yp = __shfl_up_sync(0xffffffffu, xp, o);
-    if (lane >= o) {
-      xd += yd;
-      xp += yp;
-    }
-  }
-  if (lane == 31) {
-    warp_d[warp] = xd;
-    warp_p[warp] = xp;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = nth >> 5;
-    int vd = lane < nw ? warp_d[lane] : 0, vp = lane < nw ? warp_p[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int yd = __shfl_up_sync(0xffffffffu, vd, o), yp = __shfl_up_sync(0xffffffffu, vp, o);
-      if (lane >= o) {
-        vd += yd;
-        vp += yp;
-      }
-    }
-    if (lane < nw) {
-      warp_d[lane] = vd;
-      warp_p[lane] = vp;
-    }
-  }
-  __syncthreads();
-  int run_d = xd - dsum + (warp > 0 ? warp_d[warp - 1] : 0);
-  int run_p = xp - psum + (warp > 0 ? warp_p[warp - 1] : 0);
+  int off[5], tot[5];
+  block_scan<5>(sum, off, tot);
   for (int s = s0; s < s1; ++s) {
-    int d, f;
-    counts(s, d, f);
-    p.ws.dec_off[s] = run_d;
-    p.ws.pf_off[s] = run_p;
-    const int n = __ldg(p.seq_lens + s);
-    const int t0 = __ldg(p.cu_q + s);
-    if (d > 0) {
-      const int ct = chunk_tokens(n);
-      for (int c = 0; c < d; ++c) {
-        DecodeDesc e;
-        e.s = s;
-        e.k0 = c * ct;
-        e.k1 = min(e.k0 + ct, n);
-        e.t = t0;
-        e.nchunks = d;
-        e.u0 = run_d;
-        e.c = c;
-        e.pad = 0;
-        p.ws.dec_desc[run_d + c] = e;
+    const SeqCounts c = s == s0 ? first : seq_counts(p, s, false);
+    p.ws.dec_off[s] = off[0];
+    p.ws.pf_off[s] = off[3];
+    if (c.dec > 1) p.ws.merge_list[off[4]] = s;
+    if (c.dec > 0 || c.pf > 0) {
+      const int n = __ldg(p.seq_lens + s);
+      const int t0 = __ldg(p.cu_q + s);
+      if (c.dec > 0) {
+        const int k = chunk_shift(n);
+        for (int ch = 0; ch < c.dec; ++ch) {
+          const int k0 = ch << k;
+          const int4 lo = make_int4(s, k0, min(k0 + (1 << k), n), t0);
+          const int4 hi = make_int4(c.dec, off[0], ch, 0);
+          const int slot = ch < c.full ? off[1] + ch : tot[1] + off[2];
+          int4* dst = reinterpret_cast<int4*>(p.ws.dec_desc + slot);
+          dst[0] = lo;
+          dst[1] = hi;
+        }
+      }
+      if (c.pf > 0) {
+        const int q_s = __ldg(p.cu_q + s + 1) - t0;
+        for (int qt = 0; qt < c.pf; ++qt) {
+          const int r0 = qt * kPrefillRows, r1 = min(r0 + kPrefillRows, q_s * p.G);
+          int4* dst = reinterpret_cast<int4*>(p.ws.pf_desc + off[3] + qt);
+          dst[0] = make_int4(s, t0, q_s, n);
+          dst[1] = make_int4(r0, r1, n - q_s + (r1 - 1) / p.G + 1, 0);
+        }
       }
     }
-    if (f > 0) {
-      const int q_s = __ldg(p.cu_q + s + 1) - t0;
-      for (int qt = 0; qt < f; ++qt) {
-        PrefillDesc e;
-        e.s = s;
-        e.t0 = t0;
-        e.q_s = q_s;
-        e.n = n;
-        e.r0 = qt * kPrefillRows;
-        e.r1 = min(e.r0 + kPrefillRows, q_s * p.G);
-        e.kv_end = n - q_s + (e.r1 - 1) / p.G + 1;
-        e.pad = 0;
-        p.ws.pf_desc[run_p + qt] = e;
-      }
-    }
-    run_d += d;
-    run_p += f;
+    off[0] += c.dec;
+    off[1] += c.full;
+    off[2] += c.tail;
+    off[3] += c.pf;
+    off[4] += c.dec > 1;
   }
-  if (s1 == B && s0 < s1) {
-    p.ws.dec_off[B] = run_d;
-    p.ws.pf_off[B] = run_p;
+  if (tid == 0) {
+    p.ws.dec_off[B] = tot[0];
+    p.ws.pf_off[B] = tot[3];
+    *p.ws.work = 0;
+    *p.ws.n_merge = tot[4];
   }
-  if (B == 0 && tid == 0) {
-    p.ws.dec_off[0] = 0;
-    p.ws.pf_off[0] = 0;
-  }
-  for (int i = tid; i < B * p.Hkv; i += nth) p.ws.counters[i] = 0;
-  if (tid == 0) *p.ws.work = 0;
+  for (int i = tid; i < B * p.Hkv; i += nth) p.ws.done[i] = 0;
 }
 
 // ---------------------------------------------------------------- decode
@@ -197,18 +219,101 @@ __device__ __forceinline__ int acc_d(int mt, int half, int g) {
     return 16 * mt + g + 8 * half;
 }
 
-// Byte offset, within a cache, of the HP-head row of logical token j of a
-// sequence, or -1 if its block id is out of range (recorded).
-__device__ __forceinline__ int64_t token_row(const AttnParams& p, const int32_t* bt_row, int j, int hg,
-                                             int row_bytes) {
-  const int lb = p.bs_shift >= 0 ? (j >> p.bs_shift) : (j / p.bs);
-  const int32_t blk = __ldg(bt_row + lb);
-  if (blk < 0 || blk >= p.num_blocks) {
-    atomicOr(p.err, kErrBlockRange);
-    return -1;
-  }
-  return (((int64_t)blk * p.bs + (j - lb * p.bs)) * p.Hkv + (int64_t)hg * p.hp) * (int64_t)row_bytes;
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
+
+// A warp merges the chunk results of query heads hq0 + j * stride,
+// j < nh (nh <= 4), of a split sequence: lane c holds the weights of chunks
+// c, c+32, ..; lane l accumulates output elements 4l .. 4l+3.  The loads of
+// four chunks are issued together before they are used.
+// o = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M), chunks in order.
+template <typename OutT, int D>
+__device__ __noinline__ void merge_heads(const AttnParams& p, int u0, int n, int hq0, int stride, int nh, int t,
+                                         int lane) {
+  constexpr int kQ = kMaxChunks / 32;  // chunks per lane
+  constexpr int kB = 4;                // chunks per batch of loads
+  float wv[4][kQ];
+  float inv_l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) wv[j][k] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j >= nh) break;
+    const int h = hq0 + j * stride;
+    float lv[kQ];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+      const int c = lane + 32 * k;
+      lv[k] = c < n ? __ldcg(p.ws.part_lse + (int64_t)(u0 + c) * p.Hq + h) : -INFINITY;
+      M = fmaxf(M, lv[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+      wv[j][k] = lane + 32 * k < n ? exp2f(lv[k] - M) : 0.f;
+      L += wv[j][k];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    inv_l[j] = 1.f / L;
+  }
+  const bool act = lane * 4 < D;
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* base = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)u0 * p.Hq * D) + lane;
+  const int64_t cstep = (int64_t)p.Hq * D / 4;  // float4s between chunks
+#pragma unroll
+  for (int k = 0; k < kQ; ++k) {
+    if (32 * k >= n) break;
+    for (int cb = 0; cb < 32; cb += kB) {
+      if (32 * k + cb >= n) break;
+      float4 v[kB][4];
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int c = 32 * k + cb + b;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[b][j] = (act && c < n && j < nh)
+                        ? __ldcg(base + c * cstep + (int64_t)(hq0 + j * stride) * (D / 4))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float wc = __shfl_sync(0xffffffffu, wv[j][k], cb + b);  // 0 past n
+          acc[j].x += wc * v[b][j].x;
+          acc[j].y += wc * v[b][j].y;
+          acc[j].z += wc * v[b][j].z;
+          acc[j].w += wc * v[b][j].w;
+        }
+      }
+    }
+  }
+  if (!act) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j >= nh) break;
+    OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + j * stride) * p.o_sh + 4 * lane;
+    store2(dst, acc[j].x * inv_l[j], acc[j].y * inv_l[j]);
+    store2(dst + 2, acc[j].z * inv_l[j], acc[j].w * inv_l[j]);
+  }
+}
+
+// Item descriptor as published in the item ring.
+enum : int { kItemDecode = 0, kItemMerge = 1 };
+struct ItemMeta {
+  int s, k0, k1, t, nchunks, u, hg, u0, kind;
+};
 
 template <int KV, int D, typename OutT>
 __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(AttnParams p) {
@@ -239,47 +344,96 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
     fence_barrier_init();
   }
   __syncthreads();
+  grid_dep_wait();  // the plan kernel's lists are complete from here on
   if (warp > HP) return;  // launched with (HP + 1) warps; nothing else to do
   const int HG = p.Hkv / HP;
-  const int n_items = __ldg(p.ws.dec_off + p.B) * HG;
+  const int n_dec = p.ws.dec_off[p.B] * HG;     // decode items, then
+  const int n_items = n_dec + *p.ws.n_merge * HG;  // merge items
 
   if (warp == HP) {
     // ======================= producer warp =======================
+    // Runs ahead of the consumers without waiting on global memory: the
+    // slots of 16 stages (256 tokens) are loaded a group ahead into
+    // registers (lane l serves token l % 16 of every stage: K rows on lanes
+    // 0-15, V rows on lanes 16-31).  The first item of a CTA is fixed; each
+    // later one is claimed from the work counter at the start of the
+    // current one and fetched a few stages later.  When the consumers hand
+    // an item slot back, a split chunk they finished is reported to the
+    // merge items through the sequence's done counter.
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
     const int tok = lane & 15;
     const bool is_v = lane >= 16;
     const int copy_b = HP * RowB;
+    constexpr int GS = 16;  // stages per group
     int slot = 0, phase = 0, islot = 0, iphase = 0, fills = 0;
-    int w = 0;
-    if (lane == 0) w = atomicAdd(p.ws.work, 1);
-    w = __shfl_sync(0xffffffffu, w, 0);
+    int pub0 = 0, pub1 = 0;          // items published into item slot 0 / 1
+    int done0 = -1, done1 = -1;      // done-counter index of a split chunk held by slot 0 / 1
+    // the consumers have released item slot x: report its split chunk, if any
+    auto retire = [&](int x) {
+      const int di = x ? done1 : done0;
+      if (di >= 0 && lane == 0) {
+        __threadfence();  // the consumers' partial writes (seen through the slot's mbarrier) first
+        atomicAdd(p.ws.done + di, 1);
+      }
+      if (x) done1 = -1; else done0 = -1;
+    };
+    // slot (block * bs + offset) of token `base + 16 * i + tok`, -1 past k1 or on a bad block id
+    auto load_group = [&](const DecodeDesc& e, int base, int32_t (&ids)[GS]) {
+      const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
+#pragma unroll
+      for (int i = 0; i < GS; ++i) {
+        const int j = base + ST * i + tok;
+        ids[i] = -1;
+        if (j < e.k1) {
+          const int lb = p.bs_shift >= 0 ? (j >> p.bs_shift) : (j / p.bs);
+          const int32_t blk = __ldg(bt_row + lb);
+          if (blk >= 0 && blk < p.num_blocks)
+            ids[i] = blk * p.bs + (j - lb * p.bs);
+          else
+            atomicOr(p.err, kErrBlockRange);
+        }
+      }
+    };
+    int w = blockIdx.x;
+    DecodeDesc d{};
+    int32_t ids[GS], ids_next[GS];
+    if (w < n_dec) {
+      d = p.ws.dec_desc[w / HG];
+      load_group(d, d.k0, ids);
+    }
     while (w < n_items && !flags[0]) {
-      int wn = 0;
-      if (lane == 0) wn = atomicAdd(p.ws.work, 1);  // the next item, claimed ahead
-      const DecodeDesc d = p.ws.dec_desc[w / HG];
-      const int hg = w - (w / HG) * HG;
-      // ---- publish the item: descriptor and the group's query rows
+      const bool is_dec = w < n_dec;
+      const int hg = is_dec ? w - (w / HG) * HG : (w - n_dec) % HG;
+      ItemMeta m;
+      if (is_dec) {
+        m = ItemMeta{d.s, d.k0, d.k1, d.t, d.nchunks, d.u0 + d.c, hg, d.u0, kItemDecode};
+      } else {
+        const int sm = p.ws.merge_list[(w - n_dec) / HG];
+        const int u0 = p.ws.dec_off[sm];
+        m = ItemMeta{sm, 0, 0, p.cu_q[sm], p.ws.dec_off[sm + 1] - u0, 0, hg, u0, kItemMerge};
+      }
+      // ---- publish the item: descriptor (and, for a chunk, the query rows)
       if (!mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) {
         flags[0] = 1;
         break;
       }
+      retire(islot);
+      if (is_dec && m.nchunks > 1) {
+        if (islot) done1 = m.s * HG + hg; else done0 = m.s * HG + hg;
+      }
+      if (islot) ++pub1; else ++pub0;
       unsigned char* it = items + islot * itemB;
       const int q_rows = HP * G;
       if (lane == 0) {
-        int* meta = reinterpret_cast<int*>(it + q_rows * QRowB);
-        meta[0] = d.s;
-        meta[1] = d.k0;
-        meta[2] = d.k1;
-        meta[3] = d.t;
-        meta[4] = d.nchunks;
-        meta[5] = d.u0 + d.c;
-        meta[6] = hg;
-        meta[7] = d.u0;
-        mbar_arrive_expect_tx(ifull0 + 8 * islot, q_rows * QRowB);
+        *reinterpret_cast<ItemMeta*>(it + q_rows * QRowB) = m;
+        if (is_dec)
+          mbar_arrive_expect_tx(ifull0 + 8 * islot, q_rows * QRowB);
+        else
+          mbar_arrive(ifull0 + 8 * islot);
       }
       __syncwarp();
-      {
+      if (is_dec) {
         const __nv_bfloat16* q0 = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)d.t * p.q_st +
                                   (int64_t)hg * q_rows * p.q_sh;
         if (p.q_sh == D) {
@@ -293,42 +447,83 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
         islot = 0;
         iphase ^= 1;
       }
-      // ---- K/V stages: lanes 0-15 copy K rows, lanes 16-31 V rows
-      const int32_t* bt_row = p.bt + (int64_t)d.s * p.bt_stride;
-      int64_t row_next = d.k0 + tok < d.k1 ? token_row(p, bt_row, d.k0 + tok, hg, RowB) : -1;
-      for (int j0 = d.k0; j0 < d.k1; j0 += ST) {
-        const int64_t row = row_next;
-        const int jn = j0 + ST + tok;
-        row_next = jn < d.k1 ? token_row(p, bt_row, jn, hg, RowB) : -1;  // a stage ahead
-        if (!mbar_wait(empty0 + 8 * slot, phase ^ 1, p.err)) {
-          flags[0] = 1;
-          break;
-        }
-        unsigned char* dst = smem + (size_t)slot * stageB + (is_v ? ST * tokS : 0) + tok * tokS;
-        if (row < 0) {  // past the chunk or a bad block id: this token adds nothing
-          uint4* z = reinterpret_cast<uint4*>(dst);
-          for (int i = 0; i < copy_b / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-        }
-        if (__any_sync(0xffffffffu, row < 0)) fence_proxy_async_smem();
-        const unsigned valid = __ballot_sync(0xffffffffu, row >= 0);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, __popc(valid) * copy_b);
-        __syncwarp();
-        if (row >= 0) bulk_g2s(smem_u32(dst), (is_v ? vbase : kbase) + row, copy_b, full0 + 8 * slot);
-        ++fills;
-        if (++slot == NS) {
-          slot = 0;
-          phase ^= 1;
-        }
+      int claim = 0;
+      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.work, 1);
+      if (!is_dec) {
+        w = __shfl_sync(0xffffffffu, claim, 0);
+        continue;
       }
-      w = __shfl_sync(0xffffffffu, wn, 0);
+      // ---- K/V stages, in groups of 16.  The next item's descriptor and
+      // first slots are fetched a few stages in, while the ring is full and
+      // the producer would only wait anyway.
+      const int64_t head_off = (int64_t)hg * HP;
+      const int n_stages = (d.k1 - d.k0 + ST - 1) / ST;
+      // the next item: its claim is read after stage claim_at, its
+      // descriptor load issued then and used (for its first slots) after
+      // stage fetch_at, so that no load's latency stops the producer
+      const int claim_at = min(1, n_stages - 1);
+      const int fetch_at = min(3, n_stages - 1);
+      bool failed = false;
+      int wn = n_items;
+      DecodeDesc dn{};
+      for (int gb = d.k0, st_i = 0; gb < d.k1 && !failed; gb += ST * GS) {
+        const int nb = gb + ST * GS;
+        if (nb < d.k1) load_group(d, nb, ids_next);  // this item's next group
+#pragma unroll
+        for (int i = 0; i < GS; ++i, ++st_i) {
+          const int j0 = gb + ST * i;
+          if (j0 >= d.k1) break;
+          if (!mbar_wait(empty0 + 8 * slot, phase ^ 1, p.err)) {
+            flags[0] = 1;
+            failed = true;
+            break;
+          }
+          const int32_t sl = ids[i];
+          unsigned char* dst = smem + (size_t)slot * stageB + (is_v ? ST * tokS : 0) + tok * tokS;
+          if (sl < 0) {  // past the chunk or a bad block id: this token adds nothing
+            uint4* z = reinterpret_cast<uint4*>(dst);
+            for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+          }
+          if (__any_sync(0xffffffffu, sl < 0)) fence_proxy_async_smem();
+          const unsigned valid = __ballot_sync(0xffffffffu, sl >= 0);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, __popc(valid) * copy_b);
+          __syncwarp();
+          if (sl >= 0) {
+            const int64_t off = ((int64_t)sl * p.Hkv + head_off) * RowB;
+            bulk_g2s(smem_u32(dst), (is_v ? vbase : kbase) + off, copy_b, full0 + 8 * slot);
+          }
+          ++fills;
+          if (++slot == NS) {
+            slot = 0;
+            phase ^= 1;
+          }
+          if (st_i == claim_at) {
+            wn = __shfl_sync(0xffffffffu, claim, 0);
+            if (wn < n_dec) dn = p.ws.dec_desc[wn / HG];
+          }
+          // the next item's first slots; ids_next is free unless this item
+          // still has a group to come, whose slots it holds
+          if (st_i == fetch_at && wn < n_dec && nb >= d.k1) load_group(dn, dn.k0, ids_next);
+        }
+#pragma unroll
+        for (int i = 0; i < GS; ++i) ids[i] = ids_next[i];
+        if (nb < d.k1 && nb + ST * GS >= d.k1 && wn < n_dec) load_group(dn, dn.k0, ids_next);
+      }
+      if (failed) break;
+      w = wn;
+      d = dn;
     }
-    // ---- no more items: tell the consumers, then let the last copies land
+    // ---- no more items: tell the consumers, report the last split chunks,
+    // then let the last copies land
     if (!flags[0] && mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) {
+      retire(islot);
       if (lane == 0) {
-        reinterpret_cast<int*>(items + islot * itemB + HP * G * QRowB)[0] = -1;
+        reinterpret_cast<ItemMeta*>(items + islot * itemB + HP * G * QRowB)->s = -1;
         mbar_arrive(ifull0 + 8 * islot);
       }
+      const int other = islot ^ 1, n_other = other ? pub1 : pub0;
+      if (n_other > 0 && mbar_wait(iempty0 + 8 * other, (n_other - 1) & 1, p.err)) retire(other);
     } else {
       flags[0] = 1;
     }
@@ -354,12 +549,45 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
       return;
     }
     const unsigned char* it = items + islot * itemB;
-    const int* meta = reinterpret_cast<const int*>(it + HP * G * QRowB);
-    const int s = meta[0];
-    if (s < 0) return;  // no more items
-    const int k0 = meta[1], k1 = meta[2], t = meta[3], nchunks = meta[4], u = meta[5], hg = meta[6];
-    const int u0 = meta[7];
-    const int g = hg * HP + h;  // KV head of this warp
+    const ItemMeta m = *reinterpret_cast<const ItemMeta*>(it + HP * G * QRowB);
+    if (m.s < 0) return;  // no more items
+    const int g = m.hg * HP + h;  // KV head of this warp
+    const int hq0 = g * G;
+    if (m.kind == kItemMerge) {
+      // ---- merge a split sequence's chunks once every chunk is finished
+      int ready = 1;
+      if (lane == 0) {
+        const int32_t* cnt = p.ws.done + m.s * HG + m.hg;
+        if (ld_acquire(cnt) < m.nchunks) {
+          const long long t0 = clock64();
+          while (ld_acquire(cnt) < m.nchunks) {
+            __nanosleep(200);
+            if (clock64() - t0 > kWaitLimitCycles) {
+              atomicOr(p.err, kErrWaitTimeout);
+              ready = 0;
+              break;
+            }
+          }
+        }
+      }
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      __syncwarp();
+      if (ready) {
+        // the HP warps split the group's HP * G query heads: warp h takes
+        // heads h, h + HP, .. (at most 4 each; more are done in rounds)
+        const int nq = HP * G, q0 = m.hg * nq;
+        for (int r = h; r < nq; r += 4 * HP)
+          merge_heads<OutT, D>(p, m.u0, m.nchunks, q0 + r, HP, min(4, (nq - r + HP - 1) / HP), m.t, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(iempty0 + 8 * islot);
+      if (++islot == 2) {
+        islot = 0;
+        iphase ^= 1;
+      }
+      continue;
+    }
+    const int k0 = m.k0, k1 = m.k1;
     // ---- query fragments (B operand: k = d, n = query head of the group)
     uint32_t qb[MT][2];
     {
@@ -486,8 +714,8 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
     }
     const int c0 = 2 * t4, c1 = c0 + 1;  // this thread's head columns
     const float r0 = p.v_scale / l0, r1 = p.v_scale / l1;
-    const int hq0 = g * G;
-    if (nchunks == 1) {
+    const int t = m.t, u = m.u;
+    if (m.nchunks == 1) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -514,37 +742,6 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
         if (c0 < G) p.ws.part_lse[(int64_t)u * p.Hq + hq0 + c0] = m0 + log2f(l0);
         if (c1 < G) p.ws.part_lse[(int64_t)u * p.Hq + hq0 + c1] = m1 + log2f(l1);
       }
-      // ---- the warp that finishes the last chunk of (s, g) merges them
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        __threadfence();  // cumulative over the warp's writes ordered by __syncwarp
-        last = atomicAdd(p.ws.counters + s * p.Hkv + g, 1) == nchunks - 1;
-        if (last) __threadfence();
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        for (int col = 0; col < G; ++col) {
-          const float* lse = p.ws.part_lse + (int64_t)u0 * p.Hq + hq0 + col;
-          float M = -INFINITY;
-          for (int c = lane; c < nchunks; c += 32) M = fmaxf(M, __ldcg(lse + (int64_t)c * p.Hq));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          float L = 0.f, o[D / 32];
-#pragma unroll
-          for (int k = 0; k < D / 32; ++k) o[k] = 0.f;
-          for (int c = 0; c < nchunks; ++c) {
-            const float wgt = exp2f(__ldcg(lse + (int64_t)c * p.Hq) - M);
-            L += wgt;
-            const float* src = p.ws.part_o + ((int64_t)(u0 + c) * p.Hq + hq0 + col) * D;
-#pragma unroll
-            for (int k = 0; k < D / 32; ++k) o[k] += wgt * __ldcg(src + lane + 32 * k);
-          }
-          OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + col) * p.o_sh;
-#pragma unroll
-          for (int k = 0; k < D / 32; ++k) store1(dst + lane + 32 * k, o[k] / L);
-        }
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(iempty0 + 8 * islot);
@@ -570,8 +767,7 @@ static bool decode_geometry(int Hkv, int G, int& hp, int& ns) {
 }
 
 template <int KV, int D, typename OutT>
-static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms, cudaStream_t st) {
-  using Geo = DecodeGeom<KV, D>;
+static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms, cudaStream_t st, bool pdl) {
   int hp = 1, ns = 3;
   if (!decode_geometry<KV, D>(p.Hkv, p.G, hp, ns)) return cudaErrorInvalidConfiguration;
   p.hp = hp;
@@ -585,12 +781,10 @@ static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms,
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
   if (occ < 1) occ = 1;
   int64_t grid = (int64_t)num_sms * occ;
-  const int64_t items = (max_items + hp - 1) / hp;  // max_items counts (unit, KV head) pairs
+  const int64_t items = (max_items + hp - 1) / hp + (int64_t)p.B * (p.Hkv / hp);  // chunks + merges
   if (grid > items) grid = items;
   if (grid < 1) return cudaSuccess;
-  (void)Geo::kThreads;
-  kern<<<(unsigned)grid, threads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_ex(kern, dim3((unsigned)grid), dim3(threads), smem, st, pdl, p);
 }
 
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t st) {
@@ -599,10 +793,10 @@ cudaError_t launch_plan(const AttnParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool pdl) {
 #define PKV_DEC(KV, D) \
-  (out_kind ? launch_decode_t<KV, D, __nv_bfloat16>(p, max_items, num_sms, st) \
-            : launch_decode_t<KV, D, float>(p, max_items, num_sms, st))
+  (out_kind ? launch_decode_t<KV, D, __nv_bfloat16>(p, max_items, num_sms, st, pdl) \
+            : launch_decode_t<KV, D, float>(p, max_items, num_sms, st, pdl))
   if (kv == 1) return p.D == 128 ? PKV_DEC(1, 128) : PKV_DEC(1, 64);
   return p.D == 128 ? PKV_DEC(2, 128) : PKV_DEC(2, 64);
 #undef PKV_DEC

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -57,11 +59,13 @@ struct PrefillDesc {
 };
 
 struct Workspace {
-  int32_t* dec_off;      // [B+1] prefix sums of decode chunk units
+  int32_t* dec_off;      // [B+1] prefix sums of decode chunk units (unit u0 + c = chunk c)
   int32_t* pf_off;       // [B+1] prefix sums of prefill row tiles
-  int32_t* counters;     // [B * Hkv] chunks finished per (sequence, KV head)
   int32_t* work;         // [1] next decode item to hand out
-  DecodeDesc* dec_desc;  // [B * max_chunks] decode units in order
+  int32_t* n_merge;      // [1] sequences split into more than one chunk
+  int32_t* merge_list;   // [B] those sequences
+  int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group)
+  DecodeDesc* dec_desc;  // [B * max_chunks] decode work: full chunks first, then ragged tails
   PrefillDesc* pf_desc;  // [max prefill tiles] prefill tiles in order
   float* part_o;         // [B * max_chunks, Hq, D] chunk outputs (normalised)
   float* part_lse;       // [B * max_chunks, Hq] chunk log2-sum-exp2
@@ -102,12 +106,32 @@ struct AttnParams {
 // most B * max_chunks_for(max_blocks * block_size).
 size_t attention_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_ctx);
 
+// Launch with an optional programmatic-dependent-launch attribute (the
+// kernel may start while the previous kernel of the stream finishes; it
+// must call grid_dep_wait() before reading that kernel's results).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Raises a kernel's dynamic shared memory limit once per device.
 cudaError_t set_smem_attr(const void* kernel, size_t bytes);
 
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
-                          cudaStream_t st);
+                          cudaStream_t st, bool pdl);
+
 cudaError_t launch_prefill(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
                            cudaStream_t st);
 cudaError_t launch_f32(const AttnParams& p, int out_kind, int64_t T, cudaStream_t st);
