@@ -88,28 +88,83 @@ def decode_source_hash():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clocks and throttle reasons while running."""
+    """SM clocks, power and clock-event (throttle) reasons sampled while the
+    timed region runs: NVML read through ctypes every 10 ms from a thread
+    (nothing is set, only read), else nvidia-smi every 100 ms.  Samples taken
+    before __enter__ returns are not counted."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
+        self.rows = []  # (sm_mhz, max_mhz, power_w, reasons_mask)
+        self.source = None
         self.proc = None
-        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+        self.thread = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        idx = self.gpu
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        if vis and all(x.strip().isdigit() for x in vis.split(",")):
+            idx = int(vis.split(",")[self.gpu])
+        if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex failed")
+        return lib, h
+
+    def _poll(self, lib, h):
+        import ctypes
+        sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        while not self.stop:
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+            if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) != 0:
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(rs))
+            if ok and self.armed:
+                self.rows.append((float(sm.value), float(mx.value), mw.value / 1000.0, int(rs.value)))
+            time.sleep(0.01)
 
     def __enter__(self):
+        import threading
+        self.stop, self.armed = False, False
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            lib, h = self._nvml()
+            self.thread = threading.Thread(target=self._poll, args=(lib, h), daemon=True)
+            self.thread.start()
+            self.source = "nvml 10 ms"
+        except (OSError, AttributeError, IndexError, ValueError):
+            self.thread = None
+            try:
+                self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", "100"],
+                                             stdout=self.f, stderr=subprocess.DEVNULL)
+                self.source = "nvidia-smi 100 ms"
+                t0 = time.time()
+                while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
+                    time.sleep(0.05)
+                self.skip = open(self.path).read().count("\n")
+            except (OSError, FileNotFoundError):
+                self.proc = None
+        self.armed = True
         return self
 
     def __exit__(self, *a):
+        self.armed = False
+        if self.thread is not None:
+            self.stop = True
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -117,32 +172,31 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.f.close()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            with open(self.path) as f:
+                lines = f.read().splitlines()[self.skip:]
+            os.remove(self.path)
+
+            def num(x):
+                try:
+                    return float(x)
+                except ValueError:
+                    return None
+            for line in lines:
+                r = [x.strip() for x in line.split(",")]
+                if len(r) >= 9 and num(r[1]) is not None:
+                    mask = sum(self.BITS[n] for i, n in enumerate(names) if r[5 + i].lower() == "active")
+                    self.rows.append((num(r[1]), num(r[2]) or 0.0, num(r[3]) or 0.0, mask))
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.remove(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.source}
+        reasons = sorted(n for n, b in self.BITS.items() if any(r[3] & b for r in self.rows))
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows),
+                "sm_max_mhz": max(r[1] for r in self.rows), "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": round(max(r[2] for r in self.rows), 1), "source": self.source}
 
 
 # ------------------------------------------------------------------ our arm
@@ -350,7 +404,7 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="decode")
