@@ -193,6 +193,48 @@ PKV_API pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqle
                          float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the scratch array inside the library that
+ * pkv_attention_static_workspace uses on each device (16 MiB). */
+#define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * pkv_attention_static_workspace -- pkv_attention without a workspace
+ * argument: the scratch is a fixed 16 MiB array inside the library, one per
+ * device, so the call allocates no device memory at all.  The method's
+ * description has no counterpart to this call; it exists for callers that
+ * cannot allocate: a runtime that has already handed every byte of HBM to
+ * its own pools (weights, KV block pool), plain C code with no device
+ * allocator of its own, or code that must not call cudaMalloc/cudaFree in
+ * the middle of its work because those calls can synchronise the device.
+ *
+ * Arguments, layouts, results and errors are those of pkv_attention.  In
+ * addition:
+ *   - a call whose pkv_attention_workspace_size() exceeds
+ *     PKV_STATIC_WORKSPACE_BYTES is rejected with
+ *     PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched, and
+ *     pkv_last_error() names the size it needed (as a guide: 16 sequences
+ *     with Hq = 32, D = 128 and up to 4096 tokens of context fit; 64 such
+ *     sequences do not);
+ *   - the first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before starting any stream capture;
+ *   - every call on a device uses the same array, and the array keeps what
+ *     the last call left in it (each call resets the counters it needs on
+ *     the stream before using them).  Calls whose GPU work can overlap --
+ *     issued on different streams, or from host threads with no ordering
+ *     between them -- race on the array and corrupt each other's results:
+ *     keep such calls on one stream or order them with events.
+ *   - the array's 16 MiB of device memory are reserved when the CUDA runtime
+ *     loads the library's code for this call on a device (at the first call
+ *     under lazy module loading).
+ */
+PKV_API pkv_status pkv_attention_static_workspace(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
+                                                  const pkv_tensor* seq_lens,
+                                                  const pkv_tensor* block_tables,
+                                                  const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                                                  float scale, float k_scale, float v_scale,
+                                                  int32_t max_q_len, pkv_tensor* out, void* stream);
+
 /*
  * pkv_device_errors -- synchronise the stream, then return (in *flags) and
  * clear the record of out-of-range indices the kernels met on the current

@@ -12,6 +12,8 @@ Functions (same names as the C ABI):
   pkv_attention_workspace_size(q, block_tables, k_cache)
   pkv_attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache,
                 scale, out, k_scale=1.0, v_scale=1.0, max_q_len=0, workspace=None)
+  pkv_attention_static_workspace(q, cu_seqlens_q, seq_lens, block_tables, k_cache,
+                                 v_cache, scale, out, k_scale=1.0, v_scale=1.0, max_q_len=0)
   pkv_device_errors()
 """
 import ctypes
@@ -20,12 +22,16 @@ import os
 import torch
 
 __all__ = ["PkvError", "pkv_slot_mapping", "pkv_append", "pkv_attention", "pkv_attention_workspace_size",
-           "pkv_device_errors", "pkv_version", "library_path", "load_library", "EXPORTED"]
+           "pkv_attention_static_workspace", "pkv_device_errors", "pkv_version", "library_path", "load_library",
+           "EXPORTED", "STATIC_WORKSPACE_BYTES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpkv.so")
 EXPORTED = ("pkv_slot_mapping", "pkv_append", "pkv_attention_workspace_size", "pkv_attention",
-            "pkv_device_errors", "pkv_status_string", "pkv_last_error", "pkv_version")
+            "pkv_attention_static_workspace", "pkv_device_errors", "pkv_status_string", "pkv_last_error",
+            "pkv_version")
+# PKV_STATIC_WORKSPACE_BYTES of include/pkv.h
+STATIC_WORKSPACE_BYTES = 16 << 20
 
 _DT = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.int32: 3, torch.int64: 4}
 
@@ -67,6 +73,9 @@ def load_library():
         lib.pkv_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_int32, P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         lib.pkv_attention.restype = st
+        lib.pkv_attention_static_workspace.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float,
+                                                       ctypes.c_float, ctypes.c_int32, P, ctypes.c_void_p]
+        lib.pkv_attention_static_workspace.restype = st
         lib.pkv_device_errors.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         lib.pkv_device_errors.restype = st
         lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -161,6 +170,22 @@ def pkv_attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, sca
                              float(v_scale), int(max_q_len), ctypes.byref(to),
                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
                              _stream(q.device)))
+    return out
+
+
+def pkv_attention_static_workspace(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale: float,
+                                   out, k_scale: float = 1.0, v_scale: float = 1.0, max_q_len: int = 0):
+    """pkv_attention with the library's fixed per-device scratch array as the
+    workspace: allocates nothing.  Calls on one device must not overlap."""
+    lib = load_library()
+    tq, tcu, tsl, tbt, tkc, tvc, to = (
+        _tensor(q, "q"), _tensor(cu_seqlens_q, "cu_seqlens_q"), _tensor(seq_lens, "seq_lens"),
+        _tensor(block_tables, "block_tables"), _tensor(k_cache, "k_cache"), _tensor(v_cache, "v_cache"),
+        _tensor(out, "out"))
+    _check(lib.pkv_attention_static_workspace(ctypes.byref(tq), ctypes.byref(tcu), ctypes.byref(tsl),
+                                              ctypes.byref(tbt), ctypes.byref(tkc), ctypes.byref(tvc),
+                                              float(scale), float(k_scale), float(v_scale), int(max_q_len),
+                                              ctypes.byref(to), _stream(q.device)))
     return out
 
 

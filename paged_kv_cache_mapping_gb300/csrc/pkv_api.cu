@@ -250,6 +250,8 @@ size_t attention_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, 
   return ws_layout(B, T, Hq, Hkv, D, max_ctx).total;
 }
 
+pkv_status record_failure(pkv_status st, const std::string& msg) { return fail(st, msg); }
+
 }  // namespace pkv
 
 // ======================================================================

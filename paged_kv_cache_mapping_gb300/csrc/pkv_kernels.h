@@ -6,8 +6,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
 #include <utility>
 
+#include "pkv.h"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -135,5 +137,8 @@ cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max
 cudaError_t launch_prefill(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
                            cudaStream_t st);
 cudaError_t launch_f32(const AttnParams& p, int out_kind, int64_t T, cudaStream_t st);
+
+// Records msg as the calling thread's pkv_last_error() and returns st.
+pkv_status record_failure(pkv_status st, const std::string& msg);
 
 }  // namespace pkv
