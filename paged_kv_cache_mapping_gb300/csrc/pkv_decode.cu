@@ -191,10 +191,20 @@ struct DecodeGeom {
   static constexpr int kMT = D / 16;                    // 16-wide tiles over d
   static constexpr int kQRowB = D * 2;                  // one bf16 query row
   static constexpr int kMaxHP = 8;
-  static constexpr int kThreads = (kMaxHP + 1) * 32;
+  static constexpr int kRecs = 16;  // stage records between the scheduler and the copy warp
+  static constexpr int kThreads = (kMaxHP + 2) * 32;
 };
 
 __host__ __device__ inline int align16(int v) { return (v + 15) & ~15; }
+
+// One stage as the scheduler warp hands it to the copy warp: the cache slot
+// of each of its 16 tokens (-1: nothing to copy) and the first KV head of
+// the item (-1: no more stages).
+struct StageRec {
+  int32_t slot[16];
+  int32_t head_off;
+  int32_t pad[3];
+};
 
 // Shared memory of a decode CTA: the stage ring, the item ring, mbarriers.
 template <int KV, int D>
@@ -207,7 +217,8 @@ __host__ __device__ inline int decode_item_bytes(int hp, int G) {
 }
 template <int KV, int D>
 __host__ __device__ inline size_t decode_smem(int hp, int ns, int G) {
-  return (size_t)ns * decode_stage_bytes<KV, D>(hp) + 2 * decode_item_bytes<KV, D>(hp, G) + (2 * ns + 4) * 8 + 16;
+  return (size_t)ns * decode_stage_bytes<KV, D>(hp) + 2 * decode_item_bytes<KV, D>(hp, G) +
+         DecodeGeom<KV, D>::kRecs * sizeof(StageRec) + (2 * ns + 4 + 2 * DecodeGeom<KV, D>::kRecs) * 8 + 16;
 }
 
 // Output column d of accumulator tile mt, half (0: row g, 1: row g + 8).
@@ -325,11 +336,14 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
   const int itemB = decode_item_bytes<KV, D>(HP, G);
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* items = smem + (size_t)NS * stageB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(items + 2 * itemB);
+  constexpr int NR = Geo::kRecs;
+  StageRec* recs = reinterpret_cast<StageRec*>(items + 2 * itemB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(recs + NR);
   const uint32_t stage0 = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NS;
   const uint32_t ifull0 = empty0 + 8 * NS, iempty0 = ifull0 + 16;
-  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * NS + 4);  // [0] abort
+  const uint32_t rfull0 = iempty0 + 16, rempty0 = rfull0 + 8 * NR;
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * NS + 4 + 2 * NR);  // [0] abort
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -340,36 +354,96 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
       mbar_init(ifull0 + 8 * i, 1);
       mbar_init(iempty0 + 8 * i, HP);
     }
+    for (int i = 0; i < NR; ++i) {
+      mbar_init(rfull0 + 8 * i, 32);
+      mbar_init(rempty0 + 8 * i, 32);
+    }
     flags[0] = 0;
     fence_barrier_init();
   }
   __syncthreads();
   grid_dep_wait();  // the plan kernel's lists are complete from here on
-  if (warp > HP) return;  // launched with (HP + 1) warps; nothing else to do
+  if (warp > HP + 1) return;  // launched with (HP + 2) warps; nothing else to do
   const int HG = p.Hkv / HP;
   const int n_dec = p.ws.dec_off[p.B] * HG;     // decode items, then
   const int n_items = n_dec + *p.ws.n_merge * HG;  // merge items
 
   if (warp == HP) {
-    // ======================= producer warp =======================
-    // Runs ahead of the consumers without waiting on global memory: the
-    // slots of 16 stages (256 tokens) are loaded a group ahead into
-    // registers (lane l serves token l % 16 of every stage: K rows on lanes
-    // 0-15, V rows on lanes 16-31).  The first item of a CTA is fixed; each
-    // later one is claimed from the work counter at the start of the
-    // current one and fetched a few stages later.  When the consumers hand
-    // an item slot back, a split chunk they finished is reported to the
-    // merge items through the sequence's done counter.
+    // ======================= copy warp =======================
+    // Issues the K/V copies of each stage record: lane l copies token l % 16
+    // of the stage (K rows on lanes 0-15, V rows on lanes 16-31), all HP heads
+    // of the item in one 16-byte-aligned bulk copy.  It reads no global
+    // memory itself, so nothing but a free stage slot holds it up.
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
     const int tok = lane & 15;
     const bool is_v = lane >= 16;
     const int copy_b = HP * RowB;
-    constexpr int GS = 16;  // stages per group
-    int slot = 0, phase = 0, islot = 0, iphase = 0, fills = 0;
-    int pub0 = 0, pub1 = 0;          // items published into item slot 0 / 1
-    int done0 = -1, done1 = -1;      // done-counter index of a split chunk held by slot 0 / 1
-    // the consumers have released item slot x: report its split chunk, if any
+    int rec = 0, rphase = 0, slot = 0, phase = 0, fills = 0;
+    for (;;) {
+      if (!mbar_wait(rfull0 + 8 * rec, rphase, p.err)) {
+        flags[0] = 1;
+        break;
+      }
+      const int32_t sl = recs[rec].slot[tok];
+      const int head_off = recs[rec].head_off;
+      mbar_arrive(rempty0 + 8 * rec);
+      if (++rec == NR) {
+        rec = 0;
+        rphase ^= 1;
+      }
+      if (head_off < 0) break;  // no more stages
+      if (!mbar_wait(empty0 + 8 * slot, phase ^ 1, p.err)) {
+        flags[0] = 1;
+        break;
+      }
+      unsigned char* dst = smem + (size_t)slot * stageB + (is_v ? ST * tokS : 0) + tok * tokS;
+      if (sl < 0) {  // this token adds nothing: zeros keep the MMA inputs finite
+        uint4* z = reinterpret_cast<uint4*>(dst);
+        for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+      }
+      if (__any_sync(0xffffffffu, sl < 0)) fence_proxy_async_smem();
+      const unsigned vmask = __ballot_sync(0xffffffffu, sl >= 0);
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, __popc(vmask) * copy_b);
+      __syncwarp();
+      if (sl >= 0) {
+        const int64_t off = ((int64_t)sl * p.Hkv + head_off) * RowB;
+        bulk_g2s(smem_u32(dst), (is_v ? vbase : kbase) + off, copy_b, full0 + 8 * slot);
+      }
+      ++fills;
+      if (++slot == NS) {
+        slot = 0;
+        phase ^= 1;
+      }
+    }
+    // let the last copies land before the CTA can exit
+    for (int f = 0; f < NS && f < fills; ++f) {
+      int sl = slot - 1 - f, ph = phase;
+      if (sl < 0) {
+        sl += NS;
+        ph ^= 1;
+      }
+      if (!mbar_wait(full0 + 8 * sl, ph, p.err)) break;
+    }
+    return;
+  }
+
+  if (warp == HP + 1) {
+    // ======================= scheduler warp =======================
+    // Claims items, publishes each to the consumers (descriptor and query
+    // rows) and turns its keys into stage records for the copy warp.  Every
+    // global load on the path (work counter, descriptors, block tables) is
+    // taken here, up to kRecs stages ahead of the copies, so that their
+    // latency never stalls the copy stream.  When the consumers hand an item
+    // slot back, a split chunk they finished is reported to the merge items
+    // through the sequence's done counter.
+    constexpr int GS = 16;  // stages whose block-table entries are loaded together
+    constexpr int32_t kPast = INT32_MIN;
+    const int tok = lane & 15, half = lane >> 4;
+    int rec = 0, rphase = 0;
+    int islot = 0, iphase = 0;
+    int pub0 = 0, pub1 = 0;      // items published into item slot 0 / 1
+    int done0 = -1, done1 = -1;  // done-counter index of a split chunk held by slot 0 / 1
     auto retire = [&](int x) {
       const int di = x ? done1 : done0;
       if (di >= 0 && lane == 0) {
@@ -378,63 +452,30 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
       }
       if (x) done1 = -1; else done0 = -1;
     };
-    // slot (block * bs + offset) of token `base + 16 * i + tok`, -1 past k1 or on a bad block id
-    auto load_group = [&](const DecodeDesc& e, int base, int32_t (&ids)[GS]) {
-      const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
-#pragma unroll
-      for (int i = 0; i < GS; ++i) {
-        const int j = base + ST * i + tok;
-        ids[i] = -1;
-        if (j < e.k1) {
-          const int lb = p.bs_shift >= 0 ? (j >> p.bs_shift) : (j / p.bs);
-          const int32_t blk = __ldg(bt_row + lb);
-          if (blk >= 0 && blk < p.num_blocks)
-            ids[i] = blk * p.bs + (j - lb * p.bs);
-          else
-            atomicOr(p.err, kErrBlockRange);
-        }
-      }
-    };
-    int w = blockIdx.x;
-    DecodeDesc d{};
-    int32_t ids[GS], ids_next[GS];
-    if (w < n_dec) {
-      d = p.ws.dec_desc[w / HG];
-      load_group(d, d.k0, ids);
-    }
-    while (w < n_items && !flags[0]) {
-      const bool is_dec = w < n_dec;
-      const int hg = is_dec ? w - (w / HG) * HG : (w - n_dec) % HG;
-      ItemMeta m;
-      if (is_dec) {
-        m = ItemMeta{d.s, d.k0, d.k1, d.t, d.nchunks, d.u0 + d.c, hg, d.u0, kItemDecode};
-      } else {
-        const int sm = p.ws.merge_list[(w - n_dec) / HG];
-        const int u0 = p.ws.dec_off[sm];
-        m = ItemMeta{sm, 0, 0, p.cu_q[sm], p.ws.dec_off[sm + 1] - u0, 0, hg, u0, kItemMerge};
-      }
-      // ---- publish the item: descriptor (and, for a chunk, the query rows)
-      if (!mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) {
-        flags[0] = 1;
-        break;
-      }
+    // Publishes item x (descriptor e) into the next item slot, or the end
+    // marker when x >= n_items, once the consumers have handed the slot back.
+    auto publish = [&](int x, const DecodeDesc& e) -> bool {
+      if (!mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) return false;
       retire(islot);
-      if (is_dec && m.nchunks > 1) {
-        if (islot) done1 = m.s * HG + hg; else done0 = m.s * HG + hg;
-      }
-      if (islot) ++pub1; else ++pub0;
       unsigned char* it = items + islot * itemB;
       const int q_rows = HP * G;
-      if (lane == 0) {
-        *reinterpret_cast<ItemMeta*>(it + q_rows * QRowB) = m;
-        if (is_dec)
-          mbar_arrive_expect_tx(ifull0 + 8 * islot, q_rows * QRowB);
-        else
+      ItemMeta* mp = reinterpret_cast<ItemMeta*>(it + q_rows * QRowB);
+      if (x >= n_items) {
+        if (lane == 0) {
+          mp->s = -1;
           mbar_arrive(ifull0 + 8 * islot);
-      }
-      __syncwarp();
-      if (is_dec) {
-        const __nv_bfloat16* q0 = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)d.t * p.q_st +
+        }
+      } else if (x < n_dec) {
+        const int hg = x - (x / HG) * HG;
+        if (e.nchunks > 1) {
+          if (islot) done1 = e.s * HG + hg; else done0 = e.s * HG + hg;
+        }
+        if (lane == 0) {
+          *mp = ItemMeta{e.s, e.k0, e.k1, e.t, e.nchunks, e.u0 + e.c, hg, e.u0, kItemDecode};
+          mbar_arrive_expect_tx(ifull0 + 8 * islot, q_rows * QRowB);
+        }
+        __syncwarp();
+        const __nv_bfloat16* q0 = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)e.t * p.q_st +
                                   (int64_t)hg * q_rows * p.q_sh;
         if (p.q_sh == D) {
           if (lane == 0) bulk_g2s(smem_u32(it), q0, q_rows * QRowB, ifull0 + 8 * islot);
@@ -442,99 +483,91 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
           for (int r = lane; r < q_rows; r += 32)
             bulk_g2s(smem_u32(it + r * QRowB), q0 + (int64_t)r * p.q_sh, QRowB, ifull0 + 8 * islot);
         }
+      } else {
+        const int hg = (x - n_dec) % HG;
+        const int sm = p.ws.merge_list[(x - n_dec) / HG];
+        const int u0 = p.ws.dec_off[sm];
+        const ItemMeta mm{sm, 0, 0, p.cu_q[sm], p.ws.dec_off[sm + 1] - u0, 0, hg, u0, kItemMerge};
+        if (lane == 0) {
+          *mp = mm;
+          mbar_arrive(ifull0 + 8 * islot);
+        }
       }
+      __syncwarp();
+      if (islot) ++pub1; else ++pub0;
       if (++islot == 2) {
         islot = 0;
         iphase ^= 1;
       }
+      return true;
+    };
+    // Hands one record to the copy warp; every lane arrives, releasing its
+    // own writes to the record.
+    auto put_record = [&](int tok_slot, bool writer, int head_off) -> bool {
+      if (!mbar_wait(rempty0 + 8 * rec, rphase ^ 1, p.err)) return false;
+      if (writer) recs[rec].slot[tok] = tok_slot;
+      if (lane == 0) recs[rec].head_off = head_off;
+      mbar_arrive(rfull0 + 8 * rec);
+      if (++rec == NR) {
+        rec = 0;
+        rphase ^= 1;
+      }
+      return true;
+    };
+    bool ok = true;
+    int w = blockIdx.x;
+    while (ok && w < n_items && !flags[0]) {
       int claim = 0;
-      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.work, 1);
-      if (!is_dec) {
-        w = __shfl_sync(0xffffffffu, claim, 0);
-        continue;
-      }
-      // ---- K/V stages, in groups of 16.  The next item's descriptor and
-      // first slots are fetched a few stages in, while the ring is full and
-      // the producer would only wait anyway.
-      const int64_t head_off = (int64_t)hg * HP;
-      const int n_stages = (d.k1 - d.k0 + ST - 1) / ST;
-      // the next item: its claim is read after stage claim_at, its
-      // descriptor load issued then and used (for its first slots) after
-      // stage fetch_at, so that no load's latency stops the producer
-      const int claim_at = min(1, n_stages - 1);
-      const int fetch_at = min(3, n_stages - 1);
-      bool failed = false;
-      int wn = n_items;
-      DecodeDesc dn{};
-      for (int gb = d.k0, st_i = 0; gb < d.k1 && !failed; gb += ST * GS) {
-        const int nb = gb + ST * GS;
-        if (nb < d.k1) load_group(d, nb, ids_next);  // this item's next group
+      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.work, 1);  // the next item, read at the end
+      DecodeDesc d{};
+      const bool is_dec = w < n_dec;
+      if (is_dec) d = p.ws.dec_desc[w / HG];
+      ok = publish(w, d);
+      if (ok && is_dec) {
+        const int head_off = (w - (w / HG) * HG) * HP;
+        const int32_t* bt_row = p.bt + (int64_t)d.s * p.bt_stride;
+        for (int gb = d.k0; gb < d.k1 && ok; gb += ST * GS) {
+          // lane (tok, half) resolves token tok of stages half, half + 2, ..
+          int32_t blk[GS / 2], off[GS / 2];
 #pragma unroll
-        for (int i = 0; i < GS; ++i, ++st_i) {
-          const int j0 = gb + ST * i;
-          if (j0 >= d.k1) break;
-          if (!mbar_wait(empty0 + 8 * slot, phase ^ 1, p.err)) {
-            flags[0] = 1;
-            failed = true;
-            break;
+          for (int k = 0; k < GS / 2; ++k) {
+            const int j = gb + ST * (2 * k + half) + tok;
+            blk[k] = kPast;
+            off[k] = 0;
+            if (j < d.k1) {
+              const int lb = p.bs_shift >= 0 ? (j >> p.bs_shift) : (j / p.bs);
+              off[k] = j - lb * p.bs;
+              blk[k] = __ldg(bt_row + lb);
+            }
           }
-          const int32_t sl = ids[i];
-          unsigned char* dst = smem + (size_t)slot * stageB + (is_v ? ST * tokS : 0) + tok * tokS;
-          if (sl < 0) {  // past the chunk or a bad block id: this token adds nothing
-            uint4* z = reinterpret_cast<uint4*>(dst);
-            for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+          int32_t sl[GS / 2];
+#pragma unroll
+          for (int k = 0; k < GS / 2; ++k) {
+            const bool valid = (uint32_t)blk[k] < (uint32_t)p.num_blocks;
+            if (!valid && blk[k] != kPast) atomicOr(p.err, kErrBlockRange);
+            sl[k] = valid ? blk[k] * p.bs + off[k] : -1;
           }
-          if (__any_sync(0xffffffffu, sl < 0)) fence_proxy_async_smem();
-          const unsigned valid = __ballot_sync(0xffffffffu, sl >= 0);
-          __syncwarp();
-          if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, __popc(valid) * copy_b);
-          __syncwarp();
-          if (sl >= 0) {
-            const int64_t off = ((int64_t)sl * p.Hkv + head_off) * RowB;
-            bulk_g2s(smem_u32(dst), (is_v ? vbase : kbase) + off, copy_b, full0 + 8 * slot);
+#pragma unroll
+          for (int i = 0; i < GS; ++i) {
+            if (gb + ST * i >= d.k1) break;
+            if (!put_record(sl[i >> 1], half == (i & 1), head_off)) {
+              ok = false;
+              break;
+            }
           }
-          ++fills;
-          if (++slot == NS) {
-            slot = 0;
-            phase ^= 1;
-          }
-          if (st_i == claim_at) {
-            wn = __shfl_sync(0xffffffffu, claim, 0);
-            if (wn < n_dec) dn = p.ws.dec_desc[wn / HG];
-          }
-          // the next item's first slots; ids_next is free unless this item
-          // still has a group to come, whose slots it holds
-          if (st_i == fetch_at && wn < n_dec && nb >= d.k1) load_group(dn, dn.k0, ids_next);
         }
-#pragma unroll
-        for (int i = 0; i < GS; ++i) ids[i] = ids_next[i];
-        if (nb < d.k1 && nb + ST * GS >= d.k1 && wn < n_dec) load_group(dn, dn.k0, ids_next);
       }
-      if (failed) break;
-      w = wn;
-      d = dn;
+      w = __shfl_sync(0xffffffffu, claim, 0);
     }
-    // ---- no more items: tell the consumers, report the last split chunks,
-    // then let the last copies land
-    if (!flags[0] && mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) {
-      retire(islot);
-      if (lane == 0) {
-        reinterpret_cast<ItemMeta*>(items + islot * itemB + HP * G * QRowB)->s = -1;
-        mbar_arrive(ifull0 + 8 * islot);
-      }
-      const int other = islot ^ 1, n_other = other ? pub1 : pub0;
-      if (n_other > 0 && mbar_wait(iempty0 + 8 * other, (n_other - 1) & 1, p.err)) retire(other);
+    // ---- the end: the consumers' end marker, the copy warp's end record,
+    // and the last item's split chunk reported once its slot comes back
+    if (ok && !flags[0]) ok = publish(n_items, DecodeDesc{});
+    if (!put_record(-1, true, -1)) ok = false;
+    if (ok && !flags[0]) {
+      const int n_last = islot ? pub1 : pub0;  // the slot published before the end marker
+      if (n_last > 0 && mbar_wait(iempty0 + 8 * islot, (n_last - 1) & 1, p.err)) retire(islot);
     } else {
       flags[0] = 1;
-    }
-    for (int f = 0; f < NS && f < fills; ++f) {
-      // stage slots hold the last min(NS, fills) fills; wait for each
-      int sl = slot - 1 - f, ph = phase;
-      if (sl < 0) {
-        sl += NS;
-        ph ^= 1;
-      }
-      if (!mbar_wait(full0 + 8 * sl, ph, p.err)) break;
     }
     return;
   }
@@ -776,7 +809,7 @@ static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms,
   auto kern = decode_kernel<KV, D, OutT>;
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024);
   if (e != cudaSuccess) return e;
-  const int threads = (hp + 1) * 32;
+  const int threads = (hp + 2) * 32;
   int occ = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
   if (occ < 1) occ = 1;
