@@ -510,11 +510,14 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
   }
   const int G = p.G;
   const bool prefill = (max_q_len > 1) || (max_q_len <= 0 && T >= 2) || G > p.decode_max_g;
+  const bool tc = prefill && pkv::prefill_tc_supported(kv, D, bs, G);
+  p.pf_tq = tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
   e = pkv::launch_plan(p, st);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   if (prefill) {
     const int64_t tiles = pkv::max_prefill_tiles(B, T, G);
-    e = pkv::launch_prefill(p, kv, out_kind, tiles * Hkv, sms, st);
+    e = tc ? pkv::launch_prefill_tc(p, out_kind, tiles * Hkv, sms, st)
+           : pkv::launch_prefill(p, kv, out_kind, tiles * Hkv, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (G <= p.decode_max_g) {

@@ -103,6 +103,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   return true;
 }
 
+// mbar_wait by every lane of a warp with one result for the whole warp, so
+// that no lane goes on while another gives up (warp-collective instructions
+// after the wait need every lane).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
 // 1-D bulk copy global -> shared, completion counted in bytes on an mbarrier.
 // dst, src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

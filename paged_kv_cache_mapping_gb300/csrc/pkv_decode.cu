@@ -109,7 +109,8 @@ __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool
     c.full = n >> k;
     c.tail = c.dec - c.full;
   } else {
-    c.pf = (int)(((int64_t)q_s * p.G + kPrefillRows - 1) / kPrefillRows);
+    c.pf = p.pf_tq > 0 ? (q_s + p.pf_tq - 1) / p.pf_tq
+                       : (int)(((int64_t)q_s * p.G + kPrefillRows - 1) / kPrefillRows);
   }
   return c;
 }
@@ -161,10 +162,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
       if (c.pf > 0) {
         const int q_s = __ldg(p.cu_q + s + 1) - t0;
         for (int qt = 0; qt < c.pf; ++qt) {
-          const int r0 = qt * kPrefillRows, r1 = min(r0 + kPrefillRows, q_s * p.G);
           int4* dst = reinterpret_cast<int4*>(p.ws.pf_desc + off[3] + qt);
           dst[0] = make_int4(s, t0, q_s, n);
-          dst[1] = make_int4(r0, r1, n - q_s + (r1 - 1) / p.G + 1, 0);
+          if (p.pf_tq > 0) {  // query tokens r0 .. r1-1, the last tokens (most keys) first
+            const int r1 = q_s - qt * p.pf_tq, r0 = max(0, r1 - p.pf_tq);
+            dst[1] = make_int4(r0, r1, n - q_s + r1, 0);
+          } else {  // (token, head) rows r0 .. r1-1
+            const int r0 = qt * kPrefillRows, r1 = min(r0 + kPrefillRows, q_s * p.G);
+            dst[1] = make_int4(r0, r1, n - q_s + (r1 - 1) / p.G + 1, 0);
+          }
         }
       }
     }

@@ -99,6 +99,7 @@ struct AttnParams {
   int32_t decode_max_g;  // sequences with q_s == 1 and G <= this take the decode path
   int32_t hp;            // decode: KV heads per work item (consumer warps), divides Hkv, <= 8
   int32_t ns;            // decode: stages in the staging ring
+  int32_t pf_tq;         // tensor-core prefill: query tokens per tile (0: the mma.sync prefill tiles)
   Workspace ws;
   unsigned int* err;
 };
@@ -137,6 +138,12 @@ cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max
 cudaError_t launch_prefill(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
                            cudaStream_t st);
 cudaError_t launch_f32(const AttnParams& p, int out_kind, int64_t T, cudaStream_t st);
+
+// Tensor-core (tcgen05) prefill: bf16 caches, D 64 or 128, block size a
+// multiple of 16, G <= 128.
+bool prefill_tc_supported(int kv, int64_t D, int64_t bs, int64_t G);
+int prefill_tc_tokens_per_tile(int64_t G);
+cudaError_t launch_prefill_tc(const AttnParams& p, int out_kind, int64_t max_units, int num_sms, cudaStream_t st);
 
 // Records msg as the calling thread's pkv_last_error() and returns st.
 pkv_status record_failure(pkv_status st, const std::string& msg);
