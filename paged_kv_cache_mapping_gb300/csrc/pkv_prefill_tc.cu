@@ -6,22 +6,24 @@
 // tokens of a prefill chunk attend causally over the cached prefix and the
 // chunk itself, in the same packed step as the decodes.  A tile of 128 query
 // rows (whole tokens x the G query heads of one KV head) against a tile of
-// 128 keys is a dense contraction, run here as
-//     S = Q K^T      (M 128, N 128 keys, K = D; bf16 in, fp32 in TMEM)
-//     O += P V       (M 128, N = D, K 128 keys; P split into bf16 hi + lo)
+// 64 keys is a dense contraction, run here as
+//     S = Q K^T      (M 128, N 64 keys, K = D; bf16 in, fp32 in TMEM)
+//     O += P V       (M 128, N = D, K 64 keys; P split into bf16 hi + lo)
 // with an online softmax (base 2) between them, one thread per query row.
 //
 // CTA (one per SM, persistent over tiles), 6 warps:
 //   warp 0   TMA producer: the Q tile of a work unit, then K and V tiles of
-//            128 keys (8 boxes of 16 consecutive slots of one head per d
-//            half) into 2-stage rings.  Keys past the sequence and bad block
+//            64 keys (4 boxes of 16 consecutive slots of one head per d
+//            half) into 3-stage rings.  Keys past the sequence and bad block
 //            ids read out of bounds, which TMA fills with zeros.
 //   warp 1   MMA issuer (one thread) and owner of the TMEM allocation
-//            (S: columns 0-127, O: columns 128-127+D).
-//   warps 2-5  softmax: each thread loads its row of S from TMEM, masks,
-//            updates the running max and sum, writes its row of P (hi and lo
-//            bf16 parts) into shared memory, rescales its row of O in TMEM
-//            when the max grows, and at the end writes O / l.
+//            (S double-buffered in columns 0-127, O in columns 128-127+D).
+//   warps 2-5  softmax: each thread loads its row of S from TMEM, masks it,
+//            writes its row of P (hi and lo bf16 parts) into one of two
+//            shared P buffers and, only when the row's max grows by more than
+//            2^8, waits for the previous P V and rescales its row of O in
+//            TMEM; at the end it writes O / l.  QK^T of the next tile and P V
+//            of the previous one run on the tensor core meanwhile.
 // Block sizes must be multiples of 16 (a box of 16 keys lies in one block).
 #include <cuda.h>
 
@@ -32,23 +34,28 @@
 namespace pkv {
 namespace {
 
-constexpr int kTcRows = 128;  // query rows per tile (MMA M)
-constexpr int kTcKeys = 128;  // keys per key tile
+constexpr int kTcRows = 128;    // query rows per tile (MMA M)
+constexpr int kTcKeys = 64;     // keys per key tile
+constexpr int kTcStages = 3;    // K and V ring depth
 constexpr int kTcThreads = 192;
+// A row's reference max moves only when a tile's max exceeds it by more than
+// this (log2 units), so p = 2^(x - m_ref) stays below 2^8 and O needs a
+// rescale in TMEM only then.
+constexpr float kTcTau = 8.f;
 
 template <int D>
 struct TcGeom {
   static constexpr int kHalves = D / 64;                     // 128-byte atoms along d
   static constexpr int kQBytes = kHalves * kTcRows * 128;
   static constexpr int kKVBytes = kHalves * kTcKeys * 128;   // one K or V tile
-  static constexpr int kPBytes = (kTcKeys / 64) * kTcRows * 128;
+  static constexpr int kPBytes = kTcRows * 128;              // one part (hi or lo) of a P tile: 64 keys
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;              // 2 stages
-  static constexpr int kOffV = kOffK + 2 * kKVBytes;         // 2 stages
-  static constexpr int kOffP = kOffV + 2 * kKVBytes;         // hi, then lo
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kSmem = kOffBar + 256 + 1024;          // barriers, 1024-byte alignment slack
-  static constexpr uint32_t kTmemCols = 256;                  // S 128 + O D, rounded to a power of 2
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kTcStages * kKVBytes;
+  static constexpr int kOffP = kOffV + kTcStages * kKVBytes; // [2 buffers][hi, lo]
+  static constexpr int kOffBar = kOffP + 4 * kPBytes;
+  static constexpr int kSmem = kOffBar + 512 + 1024;          // barriers, 1024-byte alignment slack
+  static constexpr uint32_t kTmemCols = 256;                  // S 2 x 64 columns, O D columns
 };
 
 // ---- tcgen05 / TMA wrappers
@@ -116,6 +123,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// p0, p1 -> bf16 pairs hi + lo: hi keeps the upper 16 bits of each fp32
+// value, lo = bf16(p - hi) rounded to nearest; hi + lo carries about 16
+// significant bits.  Element 0 in the low halves.
+__device__ __forceinline__ void split_trunc_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+  hi = __byte_perm(u0, u1, 0x7632);
+  lo = pack_bf16(p0 - __uint_as_float(u0 & 0xFFFF0000u), p1 - __uint_as_float(u1 & 0xFFFF0000u));
+}
+
 // byte offset of element (row r, column c) in a K-major, 128-byte-swizzled
 // tile of `rows` rows of 16-bit elements (64 columns per atom)
 __device__ __forceinline__ uint32_t sw128_off(int r, int c, int rows) {
@@ -124,7 +146,9 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c, int rows) {
 }
 
 // Work unit u: prefill tile u / Hkv (tokens r0 .. r1-1 of its sequence,
-// the last tokens first), KV head u % Hkv.
+// the last tokens first), KV head u % Hkv.  Key tiles are numbered across
+// the CTA's units (g); tile g uses K/V stage g % 3, S buffer g % 2, P buffer
+// g % 2 and signals o_done[g % 2] when its P V has finished.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -137,31 +161,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sV = smem_u32(smem + Geo::kOffV);
   const uint32_t sP = smem_u32(smem + Geo::kOffP);
   unsigned char* pbase = smem + Geo::kOffP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo::kOffBar);
-  const uint32_t b0 = smem_u32(bars);
-  const uint32_t q_full = b0, q_empty = b0 + 8;
-  const uint32_t k_full = b0 + 16, k_empty = b0 + 32, v_full = b0 + 48, v_empty = b0 + 64;  // [2] each
-  const uint32_t s_full = b0 + 80, s_empty = b0 + 88, p_full = b0 + 96, o_done = b0 + 104, o_free = b0 + 112;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 15);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
-  const uint32_t drain = b0 + 136;  // the MMA warp's last commit when the CTA gives up
+  const uint32_t b0 = smem_u32(smem + Geo::kOffBar);
+  auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
+  const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(22), drain = bar(23);
+  auto k_full = [&](int s) { return bar(2 + s); };
+  auto k_empty = [&](int s) { return bar(5 + s); };
+  auto v_full = [&](int s) { return bar(8 + s); };
+  auto v_empty = [&](int s) { return bar(11 + s); };
+  auto s_full = [&](int b) { return bar(14 + b); };
+  auto s_empty = [&](int b) { return bar(16 + b); };
+  auto p_full = [&](int b) { return bar(18 + b); };
+  auto o_done = [&](int b) { return bar(20 + b); };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * 24);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 25);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the abort flag as one value for the whole warp (another warp may set it
   // between two lanes' reads)
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, *abort_flag != 0); };
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(k_full + 8 * i, 1);
-      mbar_init(k_empty + 8 * i, 1);
-      mbar_init(v_full + 8 * i, 1);
-      mbar_init(v_empty + 8 * i, 1);
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, 4);
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), 4);
+      mbar_init(p_full(b), 4);
+      mbar_init(o_done(b), 1);
+    }
     mbar_init(o_free, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -176,7 +207,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tO = tmem + 2 * kTcKeys;  // S buffers: columns 0 .. 2 * kTcKeys - 1
 
   const int G = p.G, Hkv = p.Hkv;
   const int tq = p.pf_tq;  // query tokens per tile
@@ -186,23 +217,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ======================= TMA producer =======================
     const int64_t n_slots = p.num_blocks * p.bs;
-    int kv_it = 0, q_it = 0;
+    int g = 0, q_it = 0;
     for (int u = blockIdx.x; u < n_units && !aborted(); u += gridDim.x, ++q_it) {
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
-      const int g = u - (u / Hkv) * Hkv;
+      const int hk = u - (u / Hkv) * Hkv;
       if (!mbar_wait_warp(q_empty, (q_it & 1) ^ 1, p.err)) { *abort_flag = 1; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, q_box_bytes);
         for (int h = 0; h < Geo::kHalves; ++h)
-          tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, g * G, e.t0 + e.r0, q_full);
+          tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full);
       }
       const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
       const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
       bool failed = false;
-      for (int kt = 0; kt < n_kt; ++kt, ++kv_it) {
-        const int st = kv_it & 1, ph = (kv_it >> 1) & 1;
-        // lane l: key block l % 8 of the tile (16 keys), d half l / 8
-        const int bi = lane & 7, h = (lane >> 3) & 1;
+      for (int kt = 0; kt < n_kt; ++kt, ++g) {
+        const int st = g % kTcStages, ph = (g / kTcStages) & 1;
+        // lane l < 4 * halves: keys 16 (l % 4) .. +15 of the tile, d half l / 4
+        const int bi = lane & 3, h = (lane >> 2) & 1;
         const int key0 = kt * kTcKeys + 16 * bi;
         int slot = (int)n_slots;  // out of bounds: zero fill
         if (key0 < e.n) {
@@ -213,85 +244,84 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           else
             atomicOr(p.err, kErrBlockRange);
         }
-        const bool issuer = lane < 8 * Geo::kHalves;
-        if (!mbar_wait_warp(k_empty + 8 * st, ph ^ 1, p.err)) { failed = true; break; }
-        if (lane == 0) mbar_arrive_expect_tx(k_full + 8 * st, Geo::kKVBytes);
+        const bool issuer = lane < 4 * Geo::kHalves;
+        const uint32_t dst_off = st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048;
+        if (!mbar_wait_warp(k_empty(st), ph ^ 1, p.err)) { failed = true; break; }
+        if (lane == 0) mbar_arrive_expect_tx(k_full(st), Geo::kKVBytes);
         __syncwarp();
-        if (issuer)
-          tma_load_3d(sK + st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048, &tm_k, h * 64, g, slot,
-                      k_full + 8 * st);
-        if (!mbar_wait_warp(v_empty + 8 * st, ph ^ 1, p.err)) { failed = true; break; }
-        if (lane == 0) mbar_arrive_expect_tx(v_full + 8 * st, Geo::kKVBytes);
+        if (issuer) tma_load_3d(sK + dst_off, &tm_k, h * 64, hk, slot, k_full(st));
+        if (!mbar_wait_warp(v_empty(st), ph ^ 1, p.err)) { failed = true; break; }
+        if (lane == 0) mbar_arrive_expect_tx(v_full(st), Geo::kKVBytes);
         __syncwarp();
-        if (issuer)
-          tma_load_3d(sV + st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048, &tm_v, h * 64, g, slot,
-                      v_full + 8 * st);
+        if (issuer) tma_load_3d(sV + dst_off, &tm_v, h * 64, hk, slot, v_full(st));
       }
       if (failed) { *abort_flag = 1; break; }
     }
-    if (aborted() && kv_it > 0) {
+    if (aborted()) {
       // giving up: let the copies this warp issued land before the CTA exits
-      for (int k = kv_it - 1; k >= 0 && k >= kv_it - 2; --k) {
-        mbar_wait_warp(k_full + 8 * (k & 1), (k >> 1) & 1, p.err);
-        mbar_wait_warp(v_full + 8 * (k & 1), (k >> 1) & 1, p.err);
+      for (int k = g - 1; k >= 0 && k >= g - kTcStages; --k) {
+        mbar_wait_warp(k_full(k % kTcStages), (k / kTcStages) & 1, p.err);
+        mbar_wait_warp(v_full(k % kTcStages), (k / kTcStages) & 1, p.err);
       }
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     constexpr uint32_t kIdQK = umma_idesc(kTcKeys, 0);
     constexpr uint32_t kIdPV = umma_idesc(D, 1);
-    int kv_it = 0, q_it = 0, s_it = 0, p_it = 0;
+    int g = 0, q_it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok && !aborted(); u += gridDim.x, ++q_it) {
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
       ok = mbar_wait_warp(q_full, q_it & 1, p.err);
-      // S = Q K^T for key tile kt (K stage of kv_it + kt)
-      auto issue_qk = [&](int kt) -> bool {
-        const int it = kv_it + kt, st = it & 1, ph = (it >> 1) & 1;
-        if (!mbar_wait_warp(k_full + 8 * st, ph, p.err)) return false;
-        if (!mbar_wait_warp(s_empty, (s_it & 1) ^ 1, p.err)) return false;
+      // S[g % 2] = Q K^T for key tile g
+      auto issue_qk = [&](int gg) -> bool {
+        const int st = gg % kTcStages, ph = (gg / kTcStages) & 1, sb = gg & 1;
+        if (!mbar_wait_warp(k_full(st), ph, p.err)) return false;
+        if (!mbar_wait_warp(s_empty(sb), ((gg >> 1) & 1) ^ 1, p.err)) return false;
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int kb = 0; kb < D / 16; ++kb) {
-            const uint32_t ko = (kb >> 2) * kTcRows * 128 + (kb & 3) * 32;
+            const uint32_t kq = (kb >> 2) * kTcRows * 128 + (kb & 3) * 32;
             const uint32_t kk = (kb >> 2) * kTcKeys * 128 + (kb & 3) * 32;
-            umma_bf16(tS, umma_desc(sQ + ko, 16, 1024), umma_desc(sK + st * Geo::kKVBytes + kk, 16, 1024), kIdQK,
-                      kb > 0);
+            umma_bf16(tmem + sb * kTcKeys, umma_desc(sQ + kq, 16, 1024),
+                      umma_desc(sK + st * Geo::kKVBytes + kk, 16, 1024), kIdQK, kb > 0);
           }
-          umma_commit(s_full);
-          umma_commit(k_empty + 8 * st);
+          umma_commit(s_full(sb));
+          umma_commit(k_empty(st));
         }
         __syncwarp();
-        ++s_it;
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      for (int kt = 0; kt < n_kt && ok; ++kt) {
-        if (kt + 1 < n_kt) ok = issue_qk(kt + 1);
-        if (kt + 1 == n_kt && ok && lane == 0) umma_commit(q_empty);  // Q no longer read
+      if (ok) ok = issue_qk(g);
+      for (int t = 0; t < n_kt && ok; ++t) {
+        const int gg = g + t;
+        if (t + 1 < n_kt) {
+          ok = issue_qk(gg + 1);
+        } else if (lane == 0) {
+          umma_commit(q_empty);  // the unit's Q is no longer read
+        }
         if (!ok) break;
-        const int it = kv_it + kt, st = it & 1, ph = (it >> 1) & 1;
-        ok = mbar_wait_warp(p_full, p_it & 1, p.err) && mbar_wait_warp(v_full + 8 * st, ph, p.err) &&
-             (kt > 0 || mbar_wait_warp(o_free, (q_it & 1) ^ 1, p.err));
+        const int st = gg % kTcStages, ph = (gg / kTcStages) & 1, pb = gg & 1;
+        ok = mbar_wait_warp(p_full(pb), (gg >> 1) & 1, p.err) && mbar_wait_warp(v_full(st), ph, p.err) &&
+             (t > 0 || mbar_wait_warp(o_free, (q_it & 1) ^ 1, p.err));
         if (!ok) break;
-        ++p_it;
         tc_fence_after();
         if (lane == 0) {
+          const uint32_t ph_lo = sP + pb * 2 * Geo::kPBytes;
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint32_t pa = (kk >> 2) * kTcRows * 128 + (kk & 3) * 32;
             const uint64_t vd = umma_desc(sV + st * Geo::kKVBytes + kk * 2048, kTcKeys * 128, 1024);
-            umma_bf16(tO, umma_desc(sP + pa, 16, 1024), vd, kIdPV, kt > 0 || kk > 0);
-            umma_bf16(tO, umma_desc(sP + Geo::kPBytes + pa, 16, 1024), vd, kIdPV, 1);
+            umma_bf16(tO, umma_desc(ph_lo + kk * 32, 16, 1024), vd, kIdPV, t > 0 || kk > 0);
+            umma_bf16(tO, umma_desc(ph_lo + Geo::kPBytes + kk * 32, 16, 1024), vd, kIdPV, 1);
           }
-          umma_commit(o_done);
-          umma_commit(v_empty + 8 * st);
+          umma_commit(o_done(pb));
+          umma_commit(v_empty(st));
         }
         __syncwarp();
       }
-      kv_it += n_kt;
+      g += n_kt;
     }
     if (!ok || aborted()) {
       // giving up: every MMA issued so far must finish before TMEM is freed
@@ -305,112 +335,119 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int quarter = warp & 3;             // TMEM lanes 32 * quarter ..
     const int r = 32 * quarter + lane;        // this thread's query row
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    int s_it = 0, o_it = 0;
+    int g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok && !aborted(); u += gridDim.x) {
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
-      const int g = u - (u / Hkv) * Hkv;
+      const int hk = u - (u / Hkv) * Hkv;
       const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
       const int tok = r / G, hj = r - tok * G;
       const int i = e.r0 + tok;                          // query index in the sequence
       const bool valid = tok < tq && i < e.r1;
       const int pos = e.n - e.q_s + i;                   // absolute position: keys 0 .. pos
-      float m = -INFINITY, l = 0.f;
-      for (int kt = 0; kt < n_kt; ++kt) {
-        if (!mbar_wait_warp(s_full, s_it & 1, p.err)) { ok = false; break; }
-        ++s_it;
+      float m = -INFINITY, l = 0.f;                      // reference max (base 2), sum
+      for (int t = 0; t < n_kt; ++t) {
+        const int gg = g + t, sb = gg & 1;
+        if (!mbar_wait_warp(s_full(sb), (gg >> 1) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
+        // S row into registers, scaled and masked
         float x[kTcKeys];
-#pragma unroll
-        for (int c = 0; c < kTcKeys; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tS + lane_off + c, v);
+        {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + sb * kTcKeys + lane_off, v0);
+          tmem_ld32(tmem + sb * kTcKeys + lane_off + 32, v1);
           tmem_wait_ld();
+          const int lim = valid ? pos - t * kTcKeys : -1;  // columns 0 .. lim are visible
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[c + j] = __uint_as_float(v[j]);
+          for (int c = 0; c < 32; ++c) {
+            x[c] = c <= lim ? __uint_as_float(v0[c]) * p.qk_scale_log2 : -INFINITY;
+            x[c + 32] = c + 32 <= lim ? __uint_as_float(v1[c]) * p.qk_scale_log2 : -INFINITY;
+          }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty);
-        // mask and running max (base 2)
-        const int lim = valid ? pos - kt * kTcKeys : -1;  // columns 0 .. lim are visible
+        if (lane == 0) mbar_arrive(s_empty(sb));
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) {
-          x[c] = c <= lim ? x[c] * p.qk_scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
-        }
-        const float mn = fmaxf(m, mx);
-        const float ms = mn == -INFINITY ? 0.f : mn;
-        const float alpha = exp2f(m - ms);
-        float sum = 0.f;
+        for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, x[c]);
+        // move the reference max only when this tile exceeds it by more than tau
+        const bool need = mx > m + kTcTau;
+        if (__any_sync(0xffffffffu, need)) {
+          const float mn = need ? mx : m;
+          const float alpha = mn == -INFINITY ? 1.f : ex2_approx(m - mn);
+          if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // O holds every P V of the unit so far: wait for the last, rescale
+            const int pg = gg - 1;
+            if (!mbar_wait_warp(o_done(pg & 1), (pg >> 1) & 1, p.err)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t v[32];
+              tmem_ld32(tO + lane_off + c, v);
+              tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) {
-          x[c] = exp2f(x[c] - ms);
-          sum += x[c];
+              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+              tmem_st32(tO + lane_off + c, v);
+            }
+            tmem_wait_st();
+          }
+          l *= alpha;
+          m = mn;
         }
-        l = l * alpha + sum;
-        m = mn;
-        // the previous tile's P V must be done before P and O are touched
-        if (kt > 0) {
-          if (!mbar_wait_warp(o_done, o_it & 1, p.err)) { ok = false; break; }
-          ++o_it;
-          tc_fence_after();
+        // P buffer gg % 2 was last read by the P V of tile gg - 2
+        if (gg >= 2) {
+          const int pg = gg - 2;
+          if (!mbar_wait_warp(o_done(pg & 1), (pg >> 1) & 1, p.err)) { ok = false; break; }
         }
-        // P row: hi = bf16(p), lo = bf16(p - hi), 16-byte chunks in swizzled order
+        const float ms = m == -INFINITY ? 0.f : m;
+        unsigned char* pdst = pbase + (gg & 1) * 2 * Geo::kPBytes;
+        float sum = 0.f;
 #pragma unroll
         for (int c = 0; c < kTcKeys; c += 8) {
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) split_bf16(x[c + 2 * j], x[c + 2 * j + 1], hi[j], lo[j]);
-          const uint32_t off = sw128_off(r, c, kTcRows);
-          *reinterpret_cast<uint4*>(pbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(pbase + Geo::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        // rescale the rows of O whose max grew; the TMEM loads and stores are
-        // warp-collective, so the whole warp takes the branch together
-        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tO + lane_off + c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            tmem_st32(tO + lane_off + c, v);
+          for (int j = 0; j < 4; ++j) {
+            const float p0 = ex2_approx(x[c + 2 * j] - ms), p1 = ex2_approx(x[c + 2 * j + 1] - ms);
+            sum += p0 + p1;
+            split_trunc_bf16(p0, p1, hi[j], lo[j]);
           }
-          tmem_wait_st();
+          const uint32_t off = sw128_off(r, c, kTcRows);
+          *reinterpret_cast<uint4*>(pdst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(pdst + Geo::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        l += sum;
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(p_full(gg & 1));
       }
       if (!ok) break;
-      // epilogue: O / l for valid rows
-      if (!mbar_wait_warp(o_done, o_it & 1, p.err)) { ok = false; break; }
-      ++o_it;
+      // epilogue: O / l for valid rows, after the unit's last P V
+      const int lg = g + n_kt - 1;
+      if (!mbar_wait_warp(o_done(lg & 1), (lg >> 1) & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       const float inv = valid && l > 0.f ? p.v_scale / l : 0.f;
-      OutT* dst = static_cast<OutT*>(p.out) + (int64_t)(e.t0 + i) * p.o_st + (int64_t)(g * G + hj) * p.o_sh;
-#pragma unroll
+      OutT* dst = static_cast<OutT*>(p.out) + (int64_t)(e.t0 + i) * p.o_st + (int64_t)(hk * G + hj) * p.o_sh;
+#pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t v[32];
         tmem_ld32(tO + lane_off + c, v);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) store2(dst + c + j, __uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+          for (int j = 0; j < 32; j += 2)
+            store2(dst + c + j, __uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
+      g += n_kt;
     }
     if (!ok) *abort_flag = 1;
   }
-  // ---- teardown: every MMA this CTA issued has completed (the MMA warp's
-  // last commits were waited on above, or the CTA gave up), then free TMEM
+  // ---- teardown: every MMA of this CTA has completed (its results were
+  // waited for above, or the MMA warp drained them), then free TMEM
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
