@@ -235,7 +235,7 @@ static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t
   size_t n = 0;
   L.dec_off = n;  n += align_up(sizeof(int32_t) * (B + 1), 256);
   L.pf_off = n;   n += align_up(sizeof(int32_t) * (B + 1), 256);
-  L.work = n;     n += 256;  // work counter, merge count
+  L.work = n;     n += 256;  // decode work counter, merge count, prefill work counter
   L.merge_list = n; n += align_up(sizeof(int32_t) * B, 256);
   L.done = n;     n += align_up(sizeof(int32_t) * B * Hkv, 256);
   L.dec_desc = n; n += align_up(sizeof(DecodeDesc) * units, 256);
@@ -501,6 +501,7 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
     p.ws.pf_off = reinterpret_cast<int32_t*>(w + L.pf_off);
     p.ws.work = reinterpret_cast<int32_t*>(w + L.work);
     p.ws.n_merge = p.ws.work + 1;
+    p.ws.pf_work = p.ws.work + 2;
     p.ws.merge_list = reinterpret_cast<int32_t*>(w + L.merge_list);
     p.ws.done = reinterpret_cast<int32_t*>(w + L.done);
     p.ws.dec_desc = reinterpret_cast<pkv::DecodeDesc*>(w + L.dec_desc);

@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     p.ws.dec_off[B] = tot[0];
     p.ws.pf_off[B] = tot[3];
     *p.ws.work = 0;
+    *p.ws.pf_work = 0;
     *p.ws.n_merge = tot[4];
   }
   for (int i = tid; i < B * p.Hkv; i += nth) p.ws.done[i] = 0;

@@ -65,6 +65,7 @@ struct Workspace {
   int32_t* pf_off;       // [B+1] prefix sums of prefill row tiles
   int32_t* work;         // [1] next decode item to hand out
   int32_t* n_merge;      // [1] sequences split into more than one chunk
+  int32_t* pf_work;      // [1] next tensor-core prefill unit to hand out
   int32_t* merge_list;   // [B] those sequences
   int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group)
   DecodeDesc* dec_desc;  // [B * max_chunks] decode work: full chunks first, then ragged tails

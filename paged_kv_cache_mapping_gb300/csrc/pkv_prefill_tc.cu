@@ -11,11 +11,13 @@
 //     O += P V       (M 128, N = D, K 64 keys; P split into bf16 hi + lo)
 // with an online softmax (base 2) between them, one thread per query row.
 //
-// CTA (one per SM, persistent over tiles), 6 warps:
-//   warp 0   TMA producer: the Q tile of a work unit, then K and V tiles of
-//            64 keys (4 boxes of 16 consecutive slots of one head per d
-//            half) into 3-stage rings.  Keys past the sequence and bad block
-//            ids read out of bounds, which TMA fills with zeros.
+// CTA (one per SM, persistent over tiles), 7 warps:
+//   warp 0   TMA producer: claims work units, loads the Q tile of each and
+//            its K tiles of 64 keys (4 boxes of 16 consecutive slots of one
+//            head per d half) into a 3-stage ring.
+//   warp 6   TMA producer of the V tiles, in its own 3-stage ring.
+//            Keys past the sequence and bad block ids read out of bounds,
+//            which TMA fills with zeros.
 //   warp 1   MMA issuer (one thread) and owner of the TMEM allocation
 //            (S double-buffered in columns 0-127, O in columns 128-127+D).
 //   warps 2-5  softmax: each thread loads its row of S from TMEM, masks it,
@@ -37,7 +39,7 @@ namespace {
 constexpr int kTcRows = 128;    // query rows per tile (MMA M)
 constexpr int kTcKeys = 64;     // keys per key tile
 constexpr int kTcStages = 3;    // K and V ring depth
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;  // 7 warps
 // A row's reference max moves only when a tile's max exceeds it by more than
 // this (log2 units), so p = 2^(x - m_ref) stays below 2^8 and O needs a
 // rescale in TMEM only then.
@@ -129,13 +131,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// p0, p1 -> bf16 pairs hi + lo: hi keeps the upper 16 bits of each fp32
-// value, lo = bf16(p - hi) rounded to nearest; hi + lo carries about 16
-// significant bits.  Element 0 in the low halves.
+// p0, p1 >= 0 -> bf16 pairs hi + lo by truncation: hi keeps the upper 16
+// bits of each fp32 value, lo the upper 16 bits of the exact remainder
+// p - hi; hi + lo carries about 16 significant bits (relative error below
+// 2^-16) with integer and bit operations only.  Element 0 in the low halves.
 __device__ __forceinline__ void split_trunc_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
   const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
   hi = __byte_perm(u0, u1, 0x7632);
-  lo = pack_bf16(p0 - __uint_as_float(u0 & 0xFFFF0000u), p1 - __uint_as_float(u1 & 0xFFFF0000u));
+  const float r0 = p0 - __uint_as_float(u0 & 0xFFFF0000u), r1 = p1 - __uint_as_float(u1 & 0xFFFF0000u);
+  lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
 
 // byte offset of element (row r, column c) in a K-major, 128-byte-swizzled
@@ -174,6 +178,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto o_done = [&](int b) { return bar(20 + b); };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 25);
+  // work units: the TMA warp claims them and passes each index to the MMA
+  // and softmax warps through a 2-slot ring
+  auto unit_full = [&](int b) { return bar(26 + b); };
+  auto unit_empty = [&](int b) { return bar(28 + b); };
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 30);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the abort flag as one value for the whole warp (another warp may set it
   // between two lanes' reads)
@@ -195,6 +204,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(o_free, 4);
     mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(unit_full(b), 1);
+      mbar_init(unit_empty(b), 6);  // the V producer, the MMA warp and the 4 softmax warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -214,11 +227,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_units = p.ws.pf_off[p.B] * Hkv;
   const uint32_t q_box_bytes = (uint32_t)(Geo::kHalves * G * tq * 128);
 
-  if (warp == 0) {
-    // ======================= TMA producer =======================
+  // K or V tiles of one unit, one TMA box (16 keys x one d half) per lane;
+  // the block-table entry of the next tile is loaded while this one is issued
+  auto stream_kv = [&](const PrefillDesc& e, int hk, int& g, bool is_v) -> bool {
     const int64_t n_slots = p.num_blocks * p.bs;
-    int g = 0, q_it = 0;
-    for (int u = blockIdx.x; u < n_units && !aborted(); u += gridDim.x, ++q_it) {
+    const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
+    const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
+    const int bi = lane & 3, h = (lane >> 2) & 1;  // keys 16 bi .. +15 of the tile, d half h
+    const bool issuer = lane < 4 * Geo::kHalves;
+    constexpr int32_t kPast = INT32_MIN;  // a block past the sequence
+    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+    const uint32_t base = is_v ? sV : sK;
+    auto load_blk = [&](int kt) -> int32_t {
+      const int key0 = kt * kTcKeys + 16 * bi;
+      int32_t v = kPast;
+      if (key0 < e.n) v = __ldg(bt_row + (p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs)));
+      return v;
+    };
+    int32_t blk = load_blk(0);
+    for (int kt = 0; kt < n_kt; ++kt, ++g) {
+      int32_t nxt = kPast;
+      if (kt + 1 < n_kt) nxt = load_blk(kt + 1);
+      const int key0 = kt * kTcKeys + 16 * bi;
+      int slot = (int)n_slots;  // out of bounds: TMA fills zeros
+      if ((uint32_t)blk < (uint32_t)p.num_blocks) {
+        const int lb = p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs);
+        slot = blk * p.bs + (key0 - lb * p.bs);
+      } else if (blk != kPast) {
+        atomicOr(p.err, kErrBlockRange);
+      }
+      const int st = g % kTcStages, ph = (g / kTcStages) & 1;
+      const uint32_t full = is_v ? v_full(st) : k_full(st), empty = is_v ? v_empty(st) : k_empty(st);
+      if (!mbar_wait_warp(empty, ph ^ 1, p.err)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(full, Geo::kKVBytes);
+      __syncwarp();
+      if (issuer) tma_load_3d(base + st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048, map, h * 64, hk, slot, full);
+      blk = nxt;
+    }
+    return true;
+  };
+  // giving up: let the copies a producer warp issued land before the CTA exits
+  auto drain_copies = [&](int g, bool is_v) {
+    for (int k = g - 1; k >= 0 && k >= g - kTcStages; --k)
+      mbar_wait_warp(is_v ? v_full(k % kTcStages) : k_full(k % kTcStages), (k / kTcStages) & 1, p.err);
+  };
+
+  if (warp == 0) {
+    // ======================= TMA producer: units, Q and K =======================
+    int g = 0, q_it = 0, ui = 0;
+    // hands unit index x (>= n_units: no more units) to the other warps
+    auto publish = [&](int x) -> bool {
+      if (!mbar_wait_warp(unit_empty(ui & 1), ((ui >> 1) & 1) ^ 1, p.err)) return false;
+      if (lane == 0) {
+        unit_ring[ui & 1] = x;
+        mbar_arrive(unit_full(ui & 1));
+      }
+      __syncwarp();
+      ++ui;
+      return true;
+    };
+    // the first unit of a CTA is fixed; later ones are claimed in order,
+    // the longest first, one unit ahead
+    int u = blockIdx.x;
+    for (; !aborted(); ++q_it) {
+      if (!publish(u)) { *abort_flag = 1; break; }
+      if (u >= n_units) break;
+      int claim = 0;
+      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.pf_work, 1);
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int hk = u - (u / Hkv) * Hkv;
       if (!mbar_wait_warp(q_empty, (q_it & 1) ^ 1, p.err)) { *abort_flag = 1; break; }
@@ -227,50 +302,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = 0; h < Geo::kHalves; ++h)
           tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full);
       }
-      const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
-      const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
-      bool failed = false;
-      for (int kt = 0; kt < n_kt; ++kt, ++g) {
-        const int st = g % kTcStages, ph = (g / kTcStages) & 1;
-        // lane l < 4 * halves: keys 16 (l % 4) .. +15 of the tile, d half l / 4
-        const int bi = lane & 3, h = (lane >> 2) & 1;
-        const int key0 = kt * kTcKeys + 16 * bi;
-        int slot = (int)n_slots;  // out of bounds: zero fill
-        if (key0 < e.n) {
-          const int lb = p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs);
-          const int32_t blk = __ldg(bt_row + lb);
-          if ((uint32_t)blk < (uint32_t)p.num_blocks)
-            slot = blk * p.bs + (key0 - lb * p.bs);
-          else
-            atomicOr(p.err, kErrBlockRange);
-        }
-        const bool issuer = lane < 4 * Geo::kHalves;
-        const uint32_t dst_off = st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048;
-        if (!mbar_wait_warp(k_empty(st), ph ^ 1, p.err)) { failed = true; break; }
-        if (lane == 0) mbar_arrive_expect_tx(k_full(st), Geo::kKVBytes);
-        __syncwarp();
-        if (issuer) tma_load_3d(sK + dst_off, &tm_k, h * 64, hk, slot, k_full(st));
-        if (!mbar_wait_warp(v_empty(st), ph ^ 1, p.err)) { failed = true; break; }
-        if (lane == 0) mbar_arrive_expect_tx(v_full(st), Geo::kKVBytes);
-        __syncwarp();
-        if (issuer) tma_load_3d(sV + dst_off, &tm_v, h * 64, hk, slot, v_full(st));
-      }
-      if (failed) { *abort_flag = 1; break; }
+      if (!stream_kv(e, hk, g, false)) { *abort_flag = 1; break; }
+      u = __shfl_sync(0xffffffffu, claim, 0);
     }
-    if (aborted()) {
-      // giving up: let the copies this warp issued land before the CTA exits
-      for (int k = g - 1; k >= 0 && k >= g - kTcStages; --k) {
-        mbar_wait_warp(k_full(k % kTcStages), (k / kTcStages) & 1, p.err);
-        mbar_wait_warp(v_full(k % kTcStages), (k / kTcStages) & 1, p.err);
-      }
+    if (aborted()) drain_copies(g, false);
+  } else if (warp == 6) {
+    // ======================= TMA producer: V =======================
+    // runs on its own so that K tiles are not held back by the V ring
+    int g = 0, ui = 0;
+    while (!aborted()) {
+      if (!mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err)) { *abort_flag = 1; break; }
+      const int u = unit_ring[ui & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(unit_empty(ui & 1));
+      ++ui;
+      if (u >= n_units) break;
+      const PrefillDesc e = p.ws.pf_desc[u / Hkv];
+      if (!stream_kv(e, u - (u / Hkv) * Hkv, g, true)) { *abort_flag = 1; break; }
     }
+    if (aborted()) drain_copies(g, true);
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     constexpr uint32_t kIdQK = umma_idesc(kTcKeys, 0);
     constexpr uint32_t kIdPV = umma_idesc(D, 1);
-    int g = 0, q_it = 0;
+    int g = 0, q_it = 0, ui = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok && !aborted(); u += gridDim.x, ++q_it) {
+    for (; ok && !aborted(); ++q_it) {
+      int u = n_units;
+      ok = mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err);
+      if (ok) {
+        u = unit_ring[ui & 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(unit_empty(ui & 1));
+      }
+      ++ui;
+      if (!ok || u >= n_units) break;
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
       ok = mbar_wait_warp(q_full, q_it & 1, p.err);
@@ -335,9 +401,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int quarter = warp & 3;             // TMEM lanes 32 * quarter ..
     const int r = 32 * quarter + lane;        // this thread's query row
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    int g = 0;
+    int g = 0, ui = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok && !aborted(); u += gridDim.x) {
+    while (ok && !aborted()) {
+      int u = n_units;
+      ok = mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err);
+      if (ok) {
+        u = unit_ring[ui & 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(unit_empty(ui & 1));
+      }
+      ++ui;
+      if (!ok || u >= n_units) break;
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int hk = u - (u / Hkv) * Hkv;
       const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
@@ -367,9 +442,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_empty(sb));
-        float mx = -INFINITY;
+        float mx;
+        {  // tree reduction: the row is one warp lane's, so no shuffles
+          float t8[8];
 #pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, x[c]);
+          for (int j = 0; j < 8; ++j) t8[j] = x[j];
+#pragma unroll
+          for (int c = 8; c < kTcKeys; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
+          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        }
         // move the reference max only when this tile exceeds it by more than tau
         const bool need = mx > m + kTcTau;
         if (__any_sync(0xffffffffu, need)) {
@@ -401,21 +482,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const float ms = m == -INFINITY ? 0.f : m;
         unsigned char* pdst = pbase + (gg & 1) * 2 * Geo::kPBytes;
-        float sum = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums, kept apart for latency
 #pragma unroll
         for (int c = 0; c < kTcKeys; c += 8) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float p0 = ex2_approx(x[c + 2 * j] - ms), p1 = ex2_approx(x[c + 2 * j + 1] - ms);
-            sum += p0 + p1;
+            s4[j] += p0 + p1;
             split_trunc_bf16(p0, p1, hi[j], lo[j]);
           }
           const uint32_t off = sw128_off(r, c, kTcRows);
           *reinterpret_cast<uint4*>(pdst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(pdst + Geo::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        l += sum;
+        l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
