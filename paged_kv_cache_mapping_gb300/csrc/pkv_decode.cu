@@ -216,8 +216,18 @@ struct StageRec {
 // Shared memory of a decode CTA: the stage ring, the item ring, mbarriers.
 template <int KV, int D>
 __host__ __device__ inline int decode_tok_stride(int hp) { return hp * DecodeGeom<KV, D>::kRowB + 16; }
+// e4m3: tokens are staged in pairs, the two rows of a pair back to back (one
+// bulk copy of two adjacent slots fetches both) and 16 bytes of padding
+// between pairs.  bf16: one padded row per token.
 template <int KV, int D>
-__host__ __device__ inline int decode_stage_bytes(int hp) { return 2 * DecodeGeom<KV, D>::kST * decode_tok_stride<KV, D>(hp); }
+__host__ __device__ inline int decode_pair_stride(int hp) { return 2 * hp * DecodeGeom<KV, D>::kRowB + 16; }
+template <int KV, int D>
+__host__ __device__ inline int decode_half_bytes(int hp) {  // the K (or V) half of a stage
+  return KV == 2 ? (DecodeGeom<KV, D>::kST / 2) * decode_pair_stride<KV, D>(hp)
+                 : DecodeGeom<KV, D>::kST * decode_tok_stride<KV, D>(hp);
+}
+template <int KV, int D>
+__host__ __device__ inline int decode_stage_bytes(int hp) { return 2 * decode_half_bytes<KV, D>(hp); }
 template <int KV, int D>
 __host__ __device__ inline int decode_item_bytes(int hp, int G) {
   return align16(hp * G * DecodeGeom<KV, D>::kQRowB + 64);
@@ -339,6 +349,8 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
   constexpr int RowB = Geo::kRowB, ST = Geo::kST, MT = Geo::kMT, QRowB = Geo::kQRowB;
   const int HP = p.hp, NS = p.ns, G = p.G;
   const int tokS = decode_tok_stride<KV, D>(HP);
+  const int pairS = decode_pair_stride<KV, D>(HP);
+  const int halfB = decode_half_bytes<KV, D>(HP);
   const int stageB = decode_stage_bytes<KV, D>(HP);
   const int itemB = decode_item_bytes<KV, D>(HP, G);
   extern __shared__ __align__(128) unsigned char smem[];
@@ -392,7 +404,13 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
         flags[0] = 1;
         break;
       }
-      const int32_t sl = recs[rec].slot[tok];
+      // bf16: lane l copies token l % 16 (K on lanes 0-15, V on 16-31).
+      // e4m3: lane l < 16 copies pair l % 8 (K on lanes 0-7, V on 8-15).
+      const int q = lane & 7;
+      const bool pv = KV == 2 ? ((lane >> 3) & 1) != 0 : is_v;
+      const bool act = KV != 2 || lane < 16;
+      const int32_t sl = recs[rec].slot[KV == 2 ? 2 * q : tok];
+      const int32_t sl2 = KV == 2 ? recs[rec].slot[2 * q + 1] : -1;
       const int head_off = recs[rec].head_off;
       mbar_arrive(rempty0 + 8 * rec);
       if (++rec == NR) {
@@ -404,18 +422,44 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
         flags[0] = 1;
         break;
       }
-      unsigned char* dst = smem + (size_t)slot * stageB + (is_v ? ST * tokS : 0) + tok * tokS;
-      if (sl < 0) {  // this token adds nothing: zeros keep the MMA inputs finite
-        uint4* z = reinterpret_cast<uint4*>(dst);
-        for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+      const char* src = pv ? vbase : kbase;
+      unsigned char* dst = smem + (size_t)slot * stageB + (pv ? halfB : 0) + (KV == 2 ? q * pairS : tok * tokS);
+      // adjacent slots of one item covering every KV head are one contiguous run
+      const bool joint = KV == 2 && act && sl >= 0 && sl2 == sl + 1 && HP == p.Hkv;
+      int bytes = 0;
+      bool zeroed = false;
+      if (act && !joint) {
+        if (sl < 0) {  // this token adds nothing: zeros keep the MMA inputs finite
+          uint4* z = reinterpret_cast<uint4*>(dst);
+          for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+          zeroed = true;
+        } else {
+          bytes += copy_b;
+        }
+        if (KV == 2) {
+          if (sl2 < 0) {
+            uint4* z = reinterpret_cast<uint4*>(dst + copy_b);
+            for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+            zeroed = true;
+          } else {
+            bytes += copy_b;
+          }
+        }
+      } else if (joint) {
+        bytes = 2 * copy_b;
       }
-      if (__any_sync(0xffffffffu, sl < 0)) fence_proxy_async_smem();
-      const unsigned vmask = __ballot_sync(0xffffffffu, sl >= 0);
-      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, __popc(vmask) * copy_b);
+      if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
+      const unsigned total = __reduce_add_sync(0xffffffffu, (unsigned)bytes);
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, total);
       __syncwarp();
-      if (sl >= 0) {
-        const int64_t off = ((int64_t)sl * p.Hkv + head_off) * RowB;
-        bulk_g2s(smem_u32(dst), (is_v ? vbase : kbase) + off, copy_b, full0 + 8 * slot);
+      if (joint) {
+        bulk_g2s(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, 2 * copy_b, full0 + 8 * slot);
+      } else if (act) {
+        if (sl >= 0)
+          bulk_g2s(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, copy_b, full0 + 8 * slot);
+        if (KV == 2 && sl2 >= 0)
+          bulk_g2s(smem_u32(dst + copy_b), src + ((int64_t)sl2 * p.Hkv + head_off) * RowB, copy_b,
+                   full0 + 8 * slot);
       }
       ++fills;
       if (++slot == NS) {
@@ -656,11 +700,13 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
         return;
       }
       const uint32_t sK = stage0 + slot * stageB + h * RowB;
-      const uint32_t sV = sK + ST * tokS;
+      const uint32_t sV = sK + halfB;
       // ---- S = K q^T : rows = 16 tokens, cols = heads
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (KV == 2) {
-        const uint32_t aK = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * tokS + (lane >> 4) * 16;
+        // MMA row r holds token 2 (r % 8) + r / 8: each 8-row matrix reads 8
+        // different pairs, in 8 different bank groups
+        const uint32_t aK = sK + (lane & 7) * pairS + ((lane >> 3) & 1) * (HP * RowB) + (lane >> 4) * 16;
 #pragma unroll
         for (int kp = 0; kp < MT / 2; ++kp) {
           uint32_t w0, w1, w2, w3;
@@ -683,7 +729,9 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
         }
       }
       // ---- online softmax (base 2) per head column
-      const bool v0 = j0 + g4 < k1, v1 = j0 + g4 + 8 < k1;
+      // the tokens of accumulator rows g4 and g4 + 8
+      const int tr0 = KV == 2 ? 2 * g4 : g4, tr1 = KV == 2 ? 2 * g4 + 1 : g4 + 8;
+      const bool v0 = j0 + tr0 < k1, v1 = j0 + tr1 < k1;
       const float x0 = v0 ? sc[0] * p.qk_scale_log2 : -INFINITY;
       const float x1 = v0 ? sc[1] * p.qk_scale_log2 : -INFINITY;
       const float x2 = v1 ? sc[2] * p.qk_scale_log2 : -INFINITY;
@@ -710,7 +758,7 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
       // ---- O^T += V^T P : rows = d, cols = heads, k = tokens
       if constexpr (KV == 2) {
         const uint32_t b0 = movm_t(pack_f16(p0, p1)), b1 = movm_t(pack_f16(p2, p3));
-        const uint32_t aV = sV + ((lane & 7) + ((lane >> 3) & 1) * 8) * tokS + (lane >> 4) * 16;
+        const uint32_t aV = sV + (lane & 7) * pairS + ((lane >> 3) & 1) * (HP * RowB) + (lane >> 4) * 16;
 #pragma unroll
         for (int cp = 0; cp < MT / 2; ++cp) {
           uint32_t w0, w1, w2, w3;
