@@ -21,6 +21,11 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ cu_q, const int3
                                     const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
                                     int32_t B, int32_t bs, SlotT* __restrict__ slots, int64_t T,
                                     unsigned int* err) {
+  // launched with programmatic dependent launch: let the next kernel set up,
+  // then wait for the previous one (every thread, before any early return,
+  // so that this grid completes only after its predecessor)
+  launch_dependents();
+  grid_dep_wait();
   int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (t >= T) return;
   const int32_t total = __ldg(cu_q + B);
@@ -80,6 +85,8 @@ __device__ __forceinline__ uint32_t quant4(uint4 v, float inv) {
 // into 16-byte source vectors.
 template <typename SrcT, bool kFp8, typename SlotT>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  launch_dependents();  // as in slot_mapping_kernel
+  grid_dep_wait();
   constexpr int kVec = Vec16<SrcT>::n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x * (int64_t)(blockDim.x >> 5) + warp;
@@ -122,12 +129,10 @@ cudaError_t launch_slot_mapping(const int32_t* cu_q, const int32_t* seq_lens, co
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((T + threads - 1) / threads);
   if (slots_i64)
-    slot_mapping_kernel<int64_t><<<blocks, threads, 0, stream>>>(
-        cu_q, seq_lens, bt, bt_stride, max_blocks, B, bs, static_cast<int64_t*>(slots), T, err);
-  else
-    slot_mapping_kernel<int32_t><<<blocks, threads, 0, stream>>>(
-        cu_q, seq_lens, bt, bt_stride, max_blocks, B, bs, static_cast<int32_t*>(slots), T, err);
-  return cudaGetLastError();
+    return launch_ex(slot_mapping_kernel<int64_t>, dim3(blocks), dim3(threads), 0, stream, true, cu_q, seq_lens, bt,
+                     bt_stride, max_blocks, B, bs, static_cast<int64_t*>(slots), T, err);
+  return launch_ex(slot_mapping_kernel<int32_t>, dim3(blocks), dim3(threads), 0, stream, true, cu_q, seq_lens, bt,
+                   bt_stride, max_blocks, B, bs, static_cast<int32_t*>(slots), T, err);
 }
 
 cudaError_t launch_append(const AppendParams& p, int src_kind, bool fp8, bool slots_i64,
@@ -136,7 +141,8 @@ cudaError_t launch_append(const AppendParams& p, int src_kind, bool fp8, bool sl
   if (rows == 0) return cudaSuccess;
   const int threads = 256, rows_per_block = threads / 32;
   const unsigned blocks = static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block);
-#define PKV_APPEND(SRC, FP8, SLOT) append_kernel<SRC, FP8, SLOT><<<blocks, threads, 0, stream>>>(p)
+#define PKV_APPEND(SRC, FP8, SLOT) \
+  return launch_ex(append_kernel<SRC, FP8, SLOT>, dim3(blocks), dim3(threads), 0, stream, true, p)
   if (src_kind == 0) {  // f32 rows
     if (fp8) {
       if (slots_i64) PKV_APPEND(float, true, int64_t); else PKV_APPEND(float, true, int32_t);

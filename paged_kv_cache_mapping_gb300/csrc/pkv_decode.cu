@@ -122,6 +122,10 @@ __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool
 // host round trip.
 __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   launch_dependents();  // the decode kernel may start its set-up now
+  // launched with programmatic dependent launch: wait for the previous kernel
+  // (e.g. the append) before reading lengths or writing the workspace, which
+  // the previous attention call's kernels may still be reading
+  grid_dep_wait();
   const int tid = threadIdx.x, nth = blockDim.x;
   const int B = p.B;
   const int per = (B + nth - 1) / nth;
@@ -876,8 +880,7 @@ static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms,
 }
 
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_ex(plan_kernel, dim3(1), dim3(1024), 0, st, true, p);
 }
 
 cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
