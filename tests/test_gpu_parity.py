@@ -151,6 +151,35 @@ def test_head_shapes(Hq, Hkv, D):
     check_attention(out, ref, "bf16", f"Hq{Hq} Hkv{Hkv} D{D}")
 
 
+# Prefill through the tensor-core (tcgen05) kernel: bf16 caches with block
+# sizes that are multiples of 16.  Chunks with and without a cached prefix,
+# token counts that are not multiples of a tile, a decode in the same batch.
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(32, 8, 128, 16), (32, 8, 64, 32), (8, 8, 128, 64), (64, 8, 128, 16),
+                                         (48, 3, 64, 16), (12, 4, 128, 48)])
+def test_tensor_core_prefill_shapes(Hq, Hkv, D, bs):
+    wl = W.build("tc prefill", Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seq_lens=[700, 130, 1, 300, 64],
+                 q_lens=[129, 130, 1, 45, 64], src="bf16", kv="bf16", seed=2010, pool_slack=0.1)
+    ref = oracle.run_step(wl, nthreads=NT)[0]
+    ds, out = run_gpu(wl)
+    check_attention(out, ref, "bf16", f"tc prefill Hq{Hq} Hkv{Hkv} D{D} bs{bs}")
+    out16 = torch.empty(out.shape, dtype=torch.bfloat16, device=out.device)
+    ds.attention_only(out=out16)
+    torch.cuda.synchronize()
+    assert torch.equal(out16, bf16_rne_of(out))
+
+
+def test_tensor_core_prefill_layout_invariance_bitwise():
+    outs = []
+    for bs in (16, 32, 64):
+        for contiguous in (False, True):
+            wl = W.build("tc layout", Hq=32, Hkv=8, D=128, block_size=bs, seq_lens=[900, 333, 1],
+                         q_lens=[300, 333, 1], src="bf16", kv="bf16", seed=2011, contiguous=contiguous,
+                         pool_slack=0.2)
+            outs.append(run_gpu(wl)[1].cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
 def test_fp8_d64_and_prefill():
     wl = W.build("fp8 mixed", Hq=16, Hkv=4, D=64, block_size=8, seq_lens=[1, 2000, 300, 77],
                  q_lens=[1, 1, 120, 77], src="bf16", kv="e4m3", seed=2009, pool_slack=0.1)
