@@ -286,14 +286,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++ui;
       return true;
     };
-    // the first unit of a CTA is fixed; later ones are claimed in order,
-    // the longest first, one unit ahead
+    // the first unit of a CTA is fixed; later ones are claimed in order, the
+    // longest first, once this warp has issued the current unit's last K tile
+    // (a few tiles ahead of the MMAs), so that CTAs finishing early take more
     int u = blockIdx.x;
     for (; !aborted(); ++q_it) {
       if (!publish(u)) { *abort_flag = 1; break; }
       if (u >= n_units) break;
-      int claim = 0;
-      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.pf_work, 1);
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int hk = u - (u / Hkv) * Hkv;
       if (!mbar_wait_warp(q_empty, (q_it & 1) ^ 1, p.err)) { *abort_flag = 1; break; }
@@ -303,6 +302,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full);
       }
       if (!stream_kv(e, hk, g, false)) { *abort_flag = 1; break; }
+      int claim = 0;
+      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.pf_work, 1);
       u = __shfl_sync(0xffffffffu, claim, 0);
     }
     if (aborted()) drain_copies(g, false);
