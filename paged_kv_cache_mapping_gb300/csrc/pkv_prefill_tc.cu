@@ -348,12 +348,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait_warp(s_empty(sb), ((gg >> 1) & 1) ^ 1, p.err)) return false;
         tc_fence_after();
         if (lane == 0) {
+          // a descriptor's start address is its low field (bytes >> 4): the
+          // k steps add constant offsets to one base descriptor per operand
+          const uint64_t dq = umma_desc(sQ, 16, 1024), dk = umma_desc(sK + st * Geo::kKVBytes, 16, 1024);
 #pragma unroll
           for (int kb = 0; kb < D / 16; ++kb) {
-            const uint32_t kq = (kb >> 2) * kTcRows * 128 + (kb & 3) * 32;
-            const uint32_t kk = (kb >> 2) * kTcKeys * 128 + (kb & 3) * 32;
-            umma_bf16(tmem + sb * kTcKeys, umma_desc(sQ + kq, 16, 1024),
-                      umma_desc(sK + st * Geo::kKVBytes + kk, 16, 1024), kIdQK, kb > 0);
+            const uint32_t kq = ((kb >> 2) * kTcRows * 128 + (kb & 3) * 32) >> 4;
+            const uint32_t kk = ((kb >> 2) * kTcKeys * 128 + (kb & 3) * 32) >> 4;
+            umma_bf16(tmem + sb * kTcKeys, dq + kq, dk + kk, kIdQK, kb > 0);
           }
           umma_commit(s_full(sb));
           umma_commit(k_empty(st));
@@ -376,12 +378,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t ph_lo = sP + pb * 2 * Geo::kPBytes;
+          const uint64_t dp = umma_desc(sP + pb * 2 * Geo::kPBytes, 16, 1024);
+          const uint64_t dv = umma_desc(sV + st * Geo::kKVBytes, kTcKeys * 128, 1024);
+          const uint32_t acc0 = t > 0;
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint64_t vd = umma_desc(sV + st * Geo::kKVBytes + kk * 2048, kTcKeys * 128, 1024);
-            umma_bf16(tO, umma_desc(ph_lo + kk * 32, 16, 1024), vd, kIdPV, t > 0 || kk > 0);
-            umma_bf16(tO, umma_desc(ph_lo + Geo::kPBytes + kk * 32, 16, 1024), vd, kIdPV, 1);
+            umma_bf16(tO, dp + kk * 2, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);  // P hi
+            umma_bf16(tO, dp + (Geo::kPBytes >> 4) + kk * 2, dv + kk * 128, kIdPV, 1);  // P lo
           }
           umma_commit(o_done(pb));
           umma_commit(v_empty(st));
