@@ -274,6 +274,7 @@ def run_ours(args, rank, world):
     ms_step, value = job_rate(ms_step, nb["total"], world, dev)
 
     e2e = run_e2e(ds, wl, nb, args, dev, world, max_q)
+    graph = run_graph(ds, nb, args, dev, world)
     if rank != 0:
         return None
     hbm, peak_kind = peaks()
@@ -298,6 +299,7 @@ def run_ours(args, rank, world):
                      "traffic": rec["dram_bytes_per_launch"] if rec else None,
                      "algorithmic_bytes": nb["attention"], "avg_launch_us": round(attn_avg_ms * 1e3, 2)},
         "e2e": e2e,
+        "graph": graph,
         # slot mapping, append, plan, decode (+ prefill)
         "gpu_launches": (5 if max_q > 1 else 4) * args.steps,
         "clocks": clk.summary(),
@@ -305,6 +307,46 @@ def run_ours(args, rank, world):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, nb, budget_s=args.cpu_budget)
     return line
+
+
+def run_graph(ds, nb, args, dev, world):
+    """The same step replayed from CUDA graphs (one per layer cache, captured
+    after an eager warm-up): the launch cost of the four kernels goes away.
+    Reported beside the eager value, not instead of it."""
+    import torch
+    try:
+        layers = len(ds.caches)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for layer in range(layers):
+                ds.step(layer)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graphs = []
+        for layer in range(layers):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                ds.step(layer)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % layers].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        stream = torch.cuda.current_stream(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            graphs[i % layers].replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms, rate = job_rate(a.elapsed_time(b) / args.steps, nb["total"], world, dev)
+        return {"value": round(rate, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
+                "how": "the whole step replayed from a CUDA graph per layer cache"}
+    except Exception as e:  # reported, never fatal to the benchmark line
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
 
 
 def run_e2e(ds, wl, nb, args, dev, world, max_q):
