@@ -74,7 +74,8 @@ typedef enum {
   PKV_ERR_UNSUPPORTED = 2,         /* a valid request outside the built variants */
   PKV_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the size required */
   PKV_ERR_CUDA = 4,                /* a CUDA call failed; pkv_last_error() says which */
-  PKV_ERR_DEVICE_CHECK = 5         /* check mode: a kernel met an out-of-range index */
+  PKV_ERR_DEVICE_CHECK = 5,        /* check mode: a kernel met an out-of-range index */
+  PKV_ERR_OUT_OF_BLOCKS = 6        /* block manager: the pool cannot hold the request */
 } pkv_status;
 
 typedef enum {

@@ -29,7 +29,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpkv.so")
 EXPORTED = ("pkv_slot_mapping", "pkv_append", "pkv_attention_workspace_size", "pkv_attention",
             "pkv_attention_static_workspace", "pkv_device_errors", "pkv_status_string", "pkv_last_error",
-            "pkv_version")
+            "pkv_version", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_append",
+            "pkv_bm_free_sequence", "pkv_bm_block_table", "pkv_bm_build_step", "pkv_bm_stats")
 # PKV_STATIC_WORKSPACE_BYTES of include/pkv.h
 STATIC_WORKSPACE_BYTES = 16 << 20
 

@@ -265,6 +265,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_DEVICE_CHECK: return "device index check failed";
+    case PKV_ERR_OUT_OF_BLOCKS: return "out of cache blocks";
   }
   return "unknown status";
 }
