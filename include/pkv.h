@@ -117,6 +117,26 @@ PKV_API pkv_status pkv_slot_mapping(const pkv_tensor* cu_seqlens_q, const pkv_te
                             pkv_tensor* slot_mapping, void* stream);
 
 /*
+ * pkv_csr_to_block_tables -- block tables from the CSR page-list form.
+ * "How Easy Is It to Start Serving LLMs?", "1. Block-sparse KV memory:
+ * scattered pages cost nothing": a batch's pages as a sparse matrix with one
+ * row per request; request i reads pages kv_indices[kv_indptr[i] ..
+ * kv_indptr[i+1]-1] in order, and requests sharing a prompt list the same
+ * page ids.
+ *
+ *   kv_indptr     [B+1] int32 (device), non-decreasing, kv_indptr[0] = 0
+ *   kv_indices    [nnz] int32 (device), physical block ids, contiguous
+ *   block_tables  [B, max_blocks] int32 (device, written), unit column
+ *                 stride: row i holds request i's pages, then -1
+ *
+ * The sequence lengths stay the caller's (seq_lens of pkv_attention).  A
+ * row with offsets that decrease or leave [0, nnz], or with more than
+ * max_blocks pages, is filled with -1 and recorded as a device error (bit 4).
+ */
+PKV_API pkv_status pkv_csr_to_block_tables(const pkv_tensor* kv_indptr, const pkv_tensor* kv_indices,
+                                           pkv_tensor* block_tables, void* stream);
+
+/*
  * pkv_append -- scatter this step's K/V rows into their slots.
  * nanoserve, "Architecture", step 3 ("Forward": each layer writes this
  * step's K/V into the paged cache, then attends); "How to design an LLM

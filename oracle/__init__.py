@@ -17,6 +17,9 @@ statement of each definition):
                    kernel" bullets; "PageServe", "What is implemented".
   e4m3_encode / e4m3_decode / bf16_decode -- "How Easy Is It to Start Serving
                    LLMs?", "What each setting does to performance" (FP8 KV).
+  csr_to_block_tables -- "How Easy Is It to Start Serving LLMs?", "1.
+                   Block-sparse KV memory" (pages as a CSR matrix); plain
+                   Python loops, no C.
 """
 import ctypes
 import os
@@ -107,6 +110,27 @@ def e4m3_encode(x) -> np.ndarray:
     out = np.empty(x.shape, np.uint8)
     _load().orc_e4m3_encode_n(_ptr(x), _ptr(out), x.size)
     return out
+
+
+# ---------------------------------------------------------------- page lists
+def csr_to_block_tables(kv_indptr, kv_indices, max_blocks):
+    """Row i = the pages kv_indices[kv_indptr[i] .. kv_indptr[i+1]-1] in
+    order, then -1; a row whose offsets decrease or leave [0, nnz], or that
+    has more than max_blocks pages, is all -1 and flagged.
+    Returns (tables [B, max_blocks] int32, bad [B] bool)."""
+    indptr = [int(x) for x in kv_indptr]
+    indices = [int(x) for x in kv_indices]
+    B = len(indptr) - 1
+    tables = np.full((B, max_blocks), -1, np.int32)
+    bad = np.zeros(B, bool)
+    for i in range(B):
+        a, b = indptr[i], indptr[i + 1]
+        if a < 0 or b < a or b > len(indices) or b - a > max_blocks:
+            bad[i] = True
+            continue
+        for j in range(a, b):
+            tables[i, j - a] = indices[j]
+    return tables, bad
 
 
 # ---------------------------------------------------------------- slots

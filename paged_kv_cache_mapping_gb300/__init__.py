@@ -21,7 +21,7 @@ import os
 
 import torch
 
-__all__ = ["PkvError", "pkv_slot_mapping", "pkv_append", "pkv_attention", "pkv_attention_workspace_size",
+__all__ = ["PkvError", "pkv_slot_mapping", "pkv_csr_to_block_tables", "pkv_append", "pkv_attention", "pkv_attention_workspace_size",
            "pkv_attention_static_workspace", "pkv_device_errors", "pkv_version", "library_path", "load_library",
            "EXPORTED", "STATIC_WORKSPACE_BYTES"]
 
@@ -29,7 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpkv.so")
 EXPORTED = ("pkv_slot_mapping", "pkv_append", "pkv_attention_workspace_size", "pkv_attention",
             "pkv_attention_static_workspace", "pkv_device_errors", "pkv_status_string", "pkv_last_error",
-            "pkv_version", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_append",
+            "pkv_version", "pkv_csr_to_block_tables", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_append",
             "pkv_bm_free_sequence", "pkv_bm_block_table", "pkv_bm_build_step", "pkv_bm_stats")
 # PKV_STATIC_WORKSPACE_BYTES of include/pkv.h
 STATIC_WORKSPACE_BYTES = 16 << 20
@@ -67,6 +67,8 @@ def load_library():
         st = ctypes.c_int
         lib.pkv_slot_mapping.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_void_p]
         lib.pkv_slot_mapping.restype = st
+        lib.pkv_csr_to_block_tables.argtypes = [P, P, P, ctypes.c_void_p]
+        lib.pkv_csr_to_block_tables.restype = st
         lib.pkv_append.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]
         lib.pkv_append.restype = st
         lib.pkv_attention_workspace_size.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_size_t)]
@@ -135,6 +137,16 @@ def pkv_slot_mapping(cu_seqlens_q, seq_lens, block_tables, block_size: int, out=
     _check(lib.pkv_slot_mapping(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), int(block_size),
                                 ctypes.byref(o), _stream(seq_lens.device)))
     return out
+
+
+def pkv_csr_to_block_tables(kv_indptr, kv_indices, block_tables):
+    """Fills block_tables [B, max_blocks] int32 from the CSR page lists
+    (kv_indptr [B+1], kv_indices [nnz], int32); returns block_tables."""
+    lib = load_library()
+    a, b, c = (_tensor(kv_indptr, "kv_indptr"), _tensor(kv_indices, "kv_indices"),
+               _tensor(block_tables, "block_tables"))
+    _check(lib.pkv_csr_to_block_tables(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _stream(kv_indptr.device)))
+    return block_tables
 
 
 def pkv_append(k, v, slot_mapping, k_cache, v_cache, k_scale: float = 1.0, v_scale: float = 1.0):

@@ -321,6 +321,30 @@ pkv_status pkv_slot_mapping(const pkv_tensor* cu_seqlens_q, const pkv_tensor* se
   return finish(st, "pkv_slot_mapping");
 }
 
+pkv_status pkv_csr_to_block_tables(const pkv_tensor* kv_indptr, const pkv_tensor* kv_indices,
+                                   pkv_tensor* block_tables, void* stream) {
+  PKV_TRY(check_tensor("kv_indptr", kv_indptr, 1));
+  const int64_t B = kv_indptr->shape[0] - 1;
+  PKV_TRY(need(B >= 0 && B <= INT32_MAX - 1, "kv_indptr must have B + 1 entries"));
+  PKV_TRY(check_vector_i32("kv_indptr", kv_indptr, B + 1));
+  PKV_TRY(check_tensor("kv_indices", kv_indices, 1));
+  PKV_TRY(need(kv_indices->dtype == PKV_I32, "kv_indices must be int32"));
+  PKV_TRY(need(kv_indices->shape[0] <= 1 || kv_indices->stride[0] == 1, "kv_indices must be contiguous"));
+  PKV_TRY(check_block_tables(block_tables, B));
+  PKV_TRY(need(block_tables->shape[1] <= INT32_MAX, "max_blocks beyond int32"));
+  unsigned int* err = nullptr;
+  int sms = 0;
+  PKV_TRY(device_state(&err, &sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B == 0 || block_tables->shape[1] == 0) return PKV_OK;
+  cudaError_t e = pkv::launch_csr_tables(static_cast<const int32_t*>(kv_indptr->data),
+                                         static_cast<const int32_t*>(kv_indices->data), kv_indices->shape[0],
+                                         static_cast<int32_t*>(block_tables->data), block_tables->stride[0],
+                                         static_cast<int32_t>(block_tables->shape[1]), static_cast<int32_t>(B), err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "csr table launch");
+  return finish(st, "pkv_csr_to_block_tables");
+}
+
 pkv_status pkv_append(const pkv_tensor* k, const pkv_tensor* v, const pkv_tensor* slot_mapping,
                       pkv_tensor* k_cache, pkv_tensor* v_cache, float k_scale, float v_scale, void* stream) {
   PKV_TRY(check_tensor("k", k, 3));

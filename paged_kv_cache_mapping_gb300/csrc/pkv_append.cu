@@ -121,6 +121,27 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   }
 }
 
+// Block tables from the CSR page-list form: request b reads the pages
+// kv_indices[kv_indptr[b] .. kv_indptr[b+1]-1] in order ("How Easy Is It to
+// Start Serving LLMs?", "1. Block-sparse KV memory").  One block per request
+// row; a bad row (decreasing or out-of-range offsets, more pages than
+// max_blocks) is filled with -1 and recorded.
+__global__ void __launch_bounds__(128) csr_tables_kernel(const int32_t* __restrict__ indptr,
+                                                         const int32_t* __restrict__ indices, int64_t nnz,
+                                                         int32_t* __restrict__ bt, int64_t bt_stride,
+                                                         int32_t max_blocks, int32_t B, unsigned int* err) {
+  launch_dependents();
+  grid_dep_wait();
+  const int b = blockIdx.x;
+  if (b >= B) return;
+  const int32_t a0 = __ldg(indptr + b), a1 = __ldg(indptr + b + 1);
+  const bool bad = a0 < 0 || a1 < a0 || (int64_t)a1 > nnz || a1 - a0 > max_blocks;
+  if (bad && threadIdx.x == 0) atomicOr(err, kErrLengths);
+  int32_t* row = bt + (int64_t)b * bt_stride;
+  const int32_t n = bad ? 0 : a1 - a0;
+  for (int i = threadIdx.x; i < max_blocks; i += blockDim.x) row[i] = i < n ? __ldg(indices + a0 + i) : -1;
+}
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_slot_mapping(const int32_t* cu_q, const int32_t* seq_lens, const int32_t* bt,
                                 int64_t bt_stride, int32_t max_blocks, int32_t B, int32_t bs, void* slots,
@@ -133,6 +154,14 @@ cudaError_t launch_slot_mapping(const int32_t* cu_q, const int32_t* seq_lens, co
                      bt_stride, max_blocks, B, bs, static_cast<int64_t*>(slots), T, err);
   return launch_ex(slot_mapping_kernel<int32_t>, dim3(blocks), dim3(threads), 0, stream, true, cu_q, seq_lens, bt,
                    bt_stride, max_blocks, B, bs, static_cast<int32_t*>(slots), T, err);
+}
+
+cudaError_t launch_csr_tables(const int32_t* indptr, const int32_t* indices, int64_t nnz, int32_t* bt,
+                              int64_t bt_stride, int32_t max_blocks, int32_t B, unsigned int* err,
+                              cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  return launch_ex(csr_tables_kernel, dim3((unsigned)B), dim3(128), 0, stream, true, indptr, indices, nnz, bt,
+                   bt_stride, max_blocks, B, err);
 }
 
 cudaError_t launch_append(const AppendParams& p, int src_kind, bool fp8, bool slots_i64,

@@ -33,6 +33,10 @@ cudaError_t launch_slot_mapping(const int32_t* cu_q, const int32_t* seq_lens, co
                                 int64_t bt_stride, int32_t max_blocks, int32_t B, int32_t bs, void* slots,
                                 bool slots_i64, int64_t T, unsigned int* err, cudaStream_t stream);
 
+cudaError_t launch_csr_tables(const int32_t* indptr, const int32_t* indices, int64_t nnz, int32_t* bt,
+                              int64_t bt_stride, int32_t max_blocks, int32_t B, unsigned int* err,
+                              cudaStream_t stream);
+
 // src_kind: 0 = f32 rows, 1 = bf16 rows.
 cudaError_t launch_append(const AppendParams& p, int src_kind, bool fp8, bool slots_i64,
                           cudaStream_t stream);

@@ -124,6 +124,29 @@ def pin_slot_mapping(orc):
         assert np.array_equal(got, ref), bs
 
 
+# ------------------------------------------------------------ page lists
+def pin_csr_tables(orc):
+    # two requests sharing their prompt's pages 7 and 2, stored once
+    tab, bad = orc.csr_to_block_tables([0, 3, 7], [7, 2, 5, 7, 2, 9, 4], 5)
+    assert tab.tolist() == [[7, 2, 5, -1, -1], [7, 2, 9, 4, -1]] and not bad.any()
+    # round trip: tables -> CSR (one row per request, pages in order) -> tables
+    g = np.random.default_rng(12)
+    n = g.integers(0, 9, size=6)
+    tables = np.full((6, 10), -1, np.int32)
+    indptr, indices = [0], []
+    for i, k in enumerate(n):
+        pages = g.integers(0, 50, size=k)
+        tables[i, :k] = pages
+        indices += list(pages)
+        indptr.append(len(indices))
+    got, bad = orc.csr_to_block_tables(indptr, indices, 10)
+    assert np.array_equal(got, tables) and not bad.any()
+    # bad rows: decreasing offsets, too many pages, offsets past nnz
+    got, bad = orc.csr_to_block_tables([0, 2, 1, 5, 9], [1, 2, 3, 4, 5], 3)
+    assert bad.tolist() == [False, True, True, True]
+    assert got[0].tolist() == [1, 2, -1] and (got[1:] == -1).all()
+
+
 # ------------------------------------------------------------ append
 def pin_append(orc):
     g = np.random.default_rng(12)
@@ -412,7 +435,7 @@ def pin_invariant_batch(orc):
     assert np.array_equal(o_both[2:], o_sw[:1])
 
 
-ALL_PINS = [pin_bf16_decode, pin_e4m3_decode, pin_e4m3_encode, pin_slot_mapping,
+ALL_PINS = [pin_bf16_decode, pin_e4m3_decode, pin_e4m3_encode, pin_slot_mapping, pin_csr_tables,
             pin_append, pin_attention_bruteforce, pin_attention_sdpa, pin_closed_forms,
             pin_invariant_block_size_and_layout, pin_invariant_full_recompute,
             pin_invariant_shared_prefix, pin_invariant_batch]

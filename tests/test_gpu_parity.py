@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from paged_kv_cache_mapping_gb300 import (PkvError, pkv_attention, pkv_device_errors,
+from paged_kv_cache_mapping_gb300 import (PkvError, pkv_attention, pkv_csr_to_block_tables, pkv_device_errors,
                                           pkv_slot_mapping)
 from paged_kv_cache_mapping_gb300 import workloads as W
 from paged_kv_cache_mapping_gb300.harness import DeviceStep, cache_to_numpy
@@ -278,3 +278,32 @@ def test_cpu_tensors_fail_loudly():
     with pytest.raises(PkvError):
         pkv_slot_mapping(torch.zeros(5, dtype=torch.int32), torch.zeros(4, dtype=torch.int32),
                          torch.zeros(4, 4, dtype=torch.int32), 16, T=4)
+
+
+def test_csr_page_lists_give_the_same_tables_and_attention():
+    wl = W.qwen3_4b_decode(B=12, ctx=(1, 2600), block_size=16, num_blocks=0, seed=2302)
+    nb = -(-wl.seq_lens.astype(np.int64) // wl.block_size)
+    indptr = np.concatenate([[0], np.cumsum(nb)]).astype(np.int32)
+    indices = np.concatenate([wl.block_tables[i, :nb[i]] for i in range(wl.B)]).astype(np.int32)
+    max_blocks = wl.block_tables.shape[1]
+    ref, bad = oracle.csr_to_block_tables(indptr, indices, max_blocks)
+    assert not bad.any()
+    dev = torch.device("cuda")
+    bt = torch.full((wl.B, max_blocks), 12345, dtype=torch.int32, device=dev)
+    pkv_csr_to_block_tables(torch.from_numpy(indptr).to(dev), torch.from_numpy(indices).to(dev), bt)
+    torch.cuda.synchronize()
+    assert pkv_device_errors() == 0
+    assert np.array_equal(bt.cpu().numpy(), ref)
+    ds, out = run_gpu(wl)
+    ds.bt.copy_(bt)
+    out2 = ds.attention_only(out=torch.empty_like(out))
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out)
+    # bad rows: filled with -1 and recorded, never faulted
+    bad_ptr = torch.tensor([0, 3, 2, 9], dtype=torch.int32, device=dev)
+    bt2 = torch.zeros((3, 4), dtype=torch.int32, device=dev)
+    pkv_csr_to_block_tables(bad_ptr, torch.arange(6, dtype=torch.int32, device=dev), bt2)
+    torch.cuda.synchronize()
+    assert pkv_device_errors() & 4
+    ref2, bad2 = oracle.csr_to_block_tables([0, 3, 2, 9], list(range(6)), 4)
+    assert bad2.tolist() == [False, True, True] and np.array_equal(bt2.cpu().numpy(), ref2)
