@@ -56,6 +56,14 @@ def _load(path=None):
                                            P, ctypes.c_int, i32, i64, i32, i32,
                                            i32, f64, f64, f64, i64, P, P, P, i32]
         lib.orc_attention_rows.restype = ctypes.c_int
+        lib.orc_attention_v.argtypes = [P, ctypes.c_int, P, P, P, i32, i32, P, P,
+                                        ctypes.c_int, i32, i64, i32, i32, i32,
+                                        f64, f64, f64, f64, i64, P, i32]
+        lib.orc_attention_v.restype = ctypes.c_int
+        lib.orc_attention_rows_v.argtypes = [P, ctypes.c_int, P, P, P, i32, i32, P,
+                                             P, ctypes.c_int, i32, i64, i32, i32,
+                                             i32, f64, f64, f64, f64, i64, i64, P, P, P, i32]
+        lib.orc_attention_rows_v.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -167,11 +175,15 @@ def append(k, v, slots, k_cache, v_cache, k_scale=1.0, v_scale=1.0) -> None:
 
 # ---------------------------------------------------------------- attention
 def attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale,
-              k_scale=1.0, v_scale=1.0, nthreads=1, rows=None) -> np.ndarray:
+              k_scale=1.0, v_scale=1.0, nthreads=1, rows=None, soft_cap=0.0,
+              window_left=-1) -> np.ndarray:
     """fp64 attention.  q[T,Hq,D]; caches [NB,bs,Hkv,D].
 
     rows=None -> returns [T,Hq,D]; rows=(t[n], h[n]) -> returns [n, D].
+    soft_cap > 0: each scaled score s becomes soft_cap * tanh(s / soft_cap);
+    window_left >= 0: the query at position p sees keys p - window_left .. p.
     """
+    variant = soft_cap > 0 or window_left >= 0
     qf = fmt_of(q)
     q = _c(q, q.dtype)
     cu = _c(cu_seqlens_q, np.int32)
@@ -186,21 +198,37 @@ def attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale,
     lib = _load()
     if rows is None:
         out = np.zeros((T, Hq, D), np.float64)
-        rc = lib.orc_attention(_ptr(q), _FMT[qf], _ptr(cu), _ptr(sl), _ptr(bt), B,
-                               bt.shape[1], _ptr(k_cache), _ptr(v_cache),
-                               _FMT[cfmt], bs, NB, Hq, Hkv, D, float(scale),
-                               float(k_scale), float(v_scale), _ptr(out),
-                               int(nthreads))
+        if variant:
+            rc = lib.orc_attention_v(_ptr(q), _FMT[qf], _ptr(cu), _ptr(sl), _ptr(bt), B,
+                                     bt.shape[1], _ptr(k_cache), _ptr(v_cache),
+                                     _FMT[cfmt], bs, NB, Hq, Hkv, D, float(scale),
+                                     float(k_scale), float(v_scale), float(soft_cap),
+                                     int(window_left), _ptr(out), int(nthreads))
+        else:
+            rc = lib.orc_attention(_ptr(q), _FMT[qf], _ptr(cu), _ptr(sl), _ptr(bt), B,
+                                   bt.shape[1], _ptr(k_cache), _ptr(v_cache),
+                                   _FMT[cfmt], bs, NB, Hq, Hkv, D, float(scale),
+                                   float(k_scale), float(v_scale), _ptr(out),
+                                   int(nthreads))
     else:
         rt = _c(rows[0], np.int64)
         rh = _c(rows[1], np.int32)
         out = np.zeros((rt.shape[0], D), np.float64)
-        rc = lib.orc_attention_rows(_ptr(q), _FMT[qf], _ptr(cu), _ptr(sl),
-                                    _ptr(bt), B, bt.shape[1], _ptr(k_cache),
-                                    _ptr(v_cache), _FMT[cfmt], bs, NB, Hq, Hkv,
-                                    D, float(scale), float(k_scale),
-                                    float(v_scale), rt.shape[0], _ptr(rt),
-                                    _ptr(rh), _ptr(out), int(nthreads))
+        if variant:
+            rc = lib.orc_attention_rows_v(_ptr(q), _FMT[qf], _ptr(cu), _ptr(sl),
+                                          _ptr(bt), B, bt.shape[1], _ptr(k_cache),
+                                          _ptr(v_cache), _FMT[cfmt], bs, NB, Hq, Hkv,
+                                          D, float(scale), float(k_scale),
+                                          float(v_scale), float(soft_cap), int(window_left),
+                                          rt.shape[0], _ptr(rt), _ptr(rh), _ptr(out),
+                                          int(nthreads))
+        else:
+            rc = lib.orc_attention_rows(_ptr(q), _FMT[qf], _ptr(cu), _ptr(sl),
+                                        _ptr(bt), B, bt.shape[1], _ptr(k_cache),
+                                        _ptr(v_cache), _FMT[cfmt], bs, NB, Hq, Hkv,
+                                        D, float(scale), float(k_scale),
+                                        float(v_scale), rt.shape[0], _ptr(rt),
+                                        _ptr(rh), _ptr(out), int(nthreads))
     if rc:
         raise ValueError(f"attention failed ({rc})")
     return out
@@ -214,7 +242,7 @@ def cpu_count() -> int:
 
 
 # ---------------------------------------------------------------- one step
-def run_step(wl, nthreads=1, rows=None, history_batch=1 << 22):
+def run_step(wl, nthreads=1, rows=None, history_batch=1 << 22, soft_cap=0.0, window_left=-1):
     """Runs one step of a workload (see paged_kv_cache_mapping_gb300.workloads)
     on the oracle: history rows are appended first, then this step's rows are
     appended through their slots and every query row attends.
@@ -230,5 +258,6 @@ def run_step(wl, nthreads=1, rows=None, history_batch=1 << 22):
     kn, vn = wl.new_rows()
     append(kn, vn, slots, kc, vc, wl.k_scale, wl.v_scale)
     out = attention(wl.q, wl.cu_seqlens_q, wl.seq_lens, wl.block_tables, kc, vc,
-                    wl.scale, wl.k_scale, wl.v_scale, nthreads=nthreads, rows=rows)
+                    wl.scale, wl.k_scale, wl.v_scale, nthreads=nthreads, rows=rows,
+                    soft_cap=soft_cap, window_left=window_left)
     return out, kc, vc, slots

@@ -22,6 +22,9 @@
  *                        layer first writes this step's K/V into the paged
  *                        cache.
  *   orc_attention     -- causal GQA softmax attention of every packed query
+ *   (orc_attention_v, orc_attention_rows_v: the same with a logits soft cap
+ *    and a sliding window, "How Easy Is It to Start Serving LLMs?", "2. JIT
+ *    compilation: one template, a kernel per variant")
  *                        row over its sequence's pages, gathered through the
  *                        block table in logical order.
  *                        nanoserve, "Architecture" step 3 (attend over the
@@ -247,6 +250,8 @@ typedef struct {
   double* out; /* [T][Hq][D] when all rows, else [n_rows][D] */
   int32_t nthreads;
   int status;
+  double soft_cap;     /* > 0: scores s become soft_cap * tanh(s / soft_cap) */
+  int64_t window_left; /* >= 0: the query at p sees keys p - window_left .. p */
 } attn_job;
 
 /* One element of a cache, decoded to fp64 and multiplied by the per-tensor
@@ -277,25 +282,29 @@ static int attend_row(const attn_job* J, int32_t s, int32_t i, int64_t t,
   int64_t p = n_s - q_s + i;          /* absolute position of the query */
   int32_t g = h / (J->Hq / J->Hkv);   /* KV head of this query head */
   int64_t qbase = (t * J->Hq + h) * (int64_t)J->D;
-  for (int64_t j = 0; j <= p; ++j) {
+  /* visible keys: 0 .. p, or p - window_left .. p with a sliding window */
+  int64_t lo = 0;
+  if (J->window_left >= 0 && p - J->window_left > 0) lo = p - J->window_left;
+  for (int64_t j = lo; j <= p; ++j) {
     int64_t pb = J->block_tables[(int64_t)s * J->max_blocks + j / J->block_size];
     if (pb < 0 || pb >= J->num_blocks) return -1;
   }
-  /* scores, in logical key order */
+  /* scores, in logical key order; a soft cap bends each one through tanh */
   double m = -INFINITY;
-  for (int64_t j = 0; j <= p; ++j) {
+  for (int64_t j = lo; j <= p; ++j) {
     double dot = 0.0;
     for (int32_t d = 0; d < J->D; ++d)
       dot += load_src(J->q, J->q_dtype, qbase + d) *
              load_cache(J->k_cache, J->cache_dtype, kv_index(J, s, j, g, d),
                         J->k_scale);
     scores[j] = J->scale * dot;
+    if (J->soft_cap > 0.0) scores[j] = J->soft_cap * tanh(scores[j] / J->soft_cap);
     if (scores[j] > m) m = scores[j];
   }
   /* softmax weights and the weighted sum of values */
   double l = 0.0;
   for (int32_t d = 0; d < J->D; ++d) o[d] = 0.0;
-  for (int64_t j = 0; j <= p; ++j) {
+  for (int64_t j = lo; j <= p; ++j) {
     double w = exp(scores[j] - m);
     l += w;
     for (int32_t d = 0; d < J->D; ++d)
@@ -411,6 +420,44 @@ static int run_job(attn_job* J) {
   return rc;
 }
 
+/* Attention with the two variants ("How Easy Is It to Start Serving LLMs?",
+ * "2. JIT compilation: one template, a kernel per variant": a logits soft cap
+ * and a sliding window are among the variants a kernel is built for).
+ * soft_cap <= 0 and window_left < 0 turn them off. */
+int orc_attention_v(const void* q, int q_dtype, const int32_t* cu_seqlens_q,
+                    const int32_t* seq_lens, const int32_t* block_tables,
+                    int32_t B, int32_t max_blocks, const void* k_cache,
+                    const void* v_cache, int cache_dtype, int32_t block_size,
+                    int64_t num_blocks, int32_t Hq, int32_t Hkv, int32_t D,
+                    double scale, double k_scale, double v_scale,
+                    double soft_cap, int64_t window_left, double* out,
+                    int32_t nthreads) {
+  attn_job J = {q, q_dtype, cu_seqlens_q, seq_lens, block_tables, B,
+                max_blocks, block_size, k_cache, v_cache, cache_dtype,
+                num_blocks, Hq, Hkv, D, scale, k_scale, v_scale, 0, NULL,
+                NULL, out, nthreads, 0, soft_cap, window_left};
+  return run_job(&J);
+}
+
+int orc_attention_rows_v(const void* q, int q_dtype,
+                         const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                         const int32_t* block_tables, int32_t B,
+                         int32_t max_blocks, const void* k_cache,
+                         const void* v_cache, int cache_dtype,
+                         int32_t block_size, int64_t num_blocks, int32_t Hq,
+                         int32_t Hkv, int32_t D, double scale, double k_scale,
+                         double v_scale, double soft_cap, int64_t window_left,
+                         int64_t n_rows, const int64_t* rows_t,
+                         const int32_t* rows_h, double* out, int32_t nthreads) {
+  attn_job J = {q, q_dtype, cu_seqlens_q, seq_lens, block_tables, B,
+                max_blocks, block_size, k_cache, v_cache, cache_dtype,
+                num_blocks, Hq, Hkv, D, scale, k_scale, v_scale, n_rows,
+                rows_t, rows_h, out, nthreads, 0, soft_cap, window_left};
+  if (n_rows > 0 && (rows_t == NULL || rows_h == NULL)) return -2;
+  if (n_rows == 0) return 0;
+  return run_job(&J);
+}
+
 int orc_attention(const void* q, int q_dtype, const int32_t* cu_seqlens_q,
                   const int32_t* seq_lens, const int32_t* block_tables,
                   int32_t B, int32_t max_blocks, const void* k_cache,
@@ -421,7 +468,7 @@ int orc_attention(const void* q, int q_dtype, const int32_t* cu_seqlens_q,
   attn_job J = {q, q_dtype, cu_seqlens_q, seq_lens, block_tables, B,
                 max_blocks, block_size, k_cache, v_cache, cache_dtype,
                 num_blocks, Hq, Hkv, D, scale, k_scale, v_scale, 0, NULL,
-                NULL, out, nthreads, 0};
+                NULL, out, nthreads, 0, 0.0, -1};
   return run_job(&J);
 }
 
@@ -437,7 +484,7 @@ int orc_attention_rows(const void* q, int q_dtype,
   attn_job J = {q, q_dtype, cu_seqlens_q, seq_lens, block_tables, B,
                 max_blocks, block_size, k_cache, v_cache, cache_dtype,
                 num_blocks, Hq, Hkv, D, scale, k_scale, v_scale, n_rows,
-                rows_t, rows_h, out, nthreads, 0};
+                rows_t, rows_h, out, nthreads, 0, 0.0, -1};
   if (n_rows > 0 && (rows_t == NULL || rows_h == NULL)) return -2;
   if (n_rows == 0) return 0;
   return run_job(&J);

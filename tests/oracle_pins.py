@@ -435,7 +435,87 @@ def pin_invariant_batch(orc):
     assert np.array_equal(o_both[2:], o_sw[:1])
 
 
+# ------------------------------------------------------------ variants
+def _run_v(orc, P, soft_cap=0.0, window_left=-1):
+    return orc.attention(P["q"], P["cu"], P["n"], P["tab"], P["kc"], P["vc"], P["scale"],
+                         P["ks"], P["vs"], soft_cap=soft_cap, window_left=window_left)
+
+
+def pin_variants_reduce_and_window_closed_form(orc):
+    g = np.random.default_rng(15)
+    P = _random_problem(g, B=4, Hq=4, Hkv=2, D=16, bs=5, kv="bf16", src="bf16", max_n=40, max_q=6)
+    plain = _run(orc, P)
+    # a window wider than any sequence and a cap of +inf-like size change nothing
+    assert np.array_equal(_run_v(orc, P, window_left=10 ** 6), plain)
+    assert np.abs(_run_v(orc, P, soft_cap=1e12) - plain).max() <= 1e-12
+    # window 0: each query sees only its own key, so the output is its V row
+    out = _run_v(orc, P, window_left=0)
+    G = P["Hq"] // P["Hkv"]
+    for s in range(len(P["n"])):
+        K, V = _gathered(P, s)
+        N, a, b = int(P["n"][s]), int(P["cu"][s]), int(P["cu"][s + 1])
+        for i in range(b - a):
+            for h in range(P["Hq"]):
+                assert np.array_equal(out[a + i, h], V[N - (b - a) + i, h // G])
+
+
+def pin_window_sdpa(orc):
+    """torch SDPA in float64 with a banded causal mask on the gathered K/V."""
+    g = np.random.default_rng(16)
+    for W_left in (1, 3, 17):
+        P = _random_problem(g, B=4, Hq=6, Hkv=2, D=16, bs=7, kv="bf16", src="bf16", max_n=60, max_q=12)
+        out = _run_v(orc, P, window_left=W_left)
+        Q = torch.from_numpy(values(P["q"], P["src"]))
+        G = P["Hq"] // P["Hkv"]
+        for s in range(len(P["n"])):
+            a, b = int(P["cu"][s]), int(P["cu"][s + 1])
+            if b == a:
+                continue
+            K, V = _gathered(P, s)
+            K = torch.from_numpy(K).repeat_interleave(G, dim=1).transpose(0, 1)
+            V = torch.from_numpy(V).repeat_interleave(G, dim=1).transpose(0, 1)
+            N, qs = int(P["n"][s]), b - a
+            pos = (N - qs + torch.arange(qs))[:, None]
+            j = torch.arange(N)[None, :]
+            mask = (j <= pos) & (j >= pos - W_left)
+            o = torch.nn.functional.scaled_dot_product_attention(Q[a:b].transpose(0, 1), K, V,
+                                                                 attn_mask=mask, scale=P["scale"])
+            ref = o.transpose(0, 1).numpy()
+            assert np.abs(out[a:b] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max()), (W_left, s)
+
+
+def pin_soft_cap_bruteforce(orc):
+    """mpmath at 40 digits: cap * tanh(scale q.k / cap), softmax without max subtraction."""
+    g = np.random.default_rng(17)
+    mpmath.mp.dps = 40
+    for cap, W_left in ((2.0, -1), (0.7, 2)):
+        P = _random_problem(g, B=3, Hq=4, Hkv=2, D=6, bs=3, kv="bf16", src="bf16", max_n=8, scale=1.3)
+        out = _run_v(orc, P, soft_cap=cap, window_left=W_left)
+        Q = values(P["q"], P["src"])
+        G = P["Hq"] // P["Hkv"]
+        for s in range(3):
+            K, V = _gathered(P, s)
+            N, a, b = int(P["n"][s]), int(P["cu"][s]), int(P["cu"][s + 1])
+            for i in range(b - a):
+                pos = N - (b - a) + i
+                lo = 0 if W_left < 0 else max(0, pos - W_left)
+                for h in range(P["Hq"]):
+                    kh = h // G
+                    w = []
+                    for j in range(lo, pos + 1):
+                        dot = mpmath.fsum(mpmath.mpf(float(Q[a + i, h, d])) * mpmath.mpf(float(K[j, kh, d]))
+                                          for d in range(Q.shape[2]))
+                        sc = mpmath.mpf(cap) * mpmath.tanh(mpmath.mpf(P["scale"]) * dot / mpmath.mpf(cap))
+                        w.append(mpmath.exp(sc))
+                    den = mpmath.fsum(w)
+                    for d in range(Q.shape[2]):
+                        num = mpmath.fsum(w[j - lo] * mpmath.mpf(float(V[j, kh, d])) for j in range(lo, pos + 1))
+                        ref = float(num / den)
+                        assert abs(out[a + i, h, d] - ref) <= 1e-12 * max(1.0, abs(ref)), (cap, W_left, s, i, h, d)
+
+
 ALL_PINS = [pin_bf16_decode, pin_e4m3_decode, pin_e4m3_encode, pin_slot_mapping, pin_csr_tables,
             pin_append, pin_attention_bruteforce, pin_attention_sdpa, pin_closed_forms,
             pin_invariant_block_size_and_layout, pin_invariant_full_recompute,
-            pin_invariant_shared_prefix, pin_invariant_batch]
+            pin_invariant_shared_prefix, pin_invariant_batch, pin_variants_reduce_and_window_closed_form,
+            pin_window_sdpa, pin_soft_cap_bruteforce]

@@ -35,6 +35,9 @@ MISTAKES = [
     ("q/k operand transposed", "load_src(J->q, J->q_dtype, qbase + d) *",
      "load_src(J->q, J->q_dtype, qbase + (J->D - 1 - d)) *"),
     ("max over keys skipped", "if (scores[j] > m) m = scores[j];", "m = scores[0];"),
+    ("sliding window off by one", "lo = p - J->window_left;", "lo = p - J->window_left + 1;"),
+    ("soft cap on the unscaled dot", "scores[j] = J->soft_cap * tanh(scores[j] / J->soft_cap);",
+     "scores[j] = J->soft_cap * tanh(dot / J->soft_cap);"),
 ]
 
 
