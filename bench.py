@@ -40,14 +40,20 @@ DECODE_SOURCES = ["pkv_decode.cu", "pkv_pipeline.cuh", "pkv_common.cuh"]
 
 
 # ------------------------------------------------------------------ accounting
-def step_bytes(wl, out_bytes=2):
+def step_bytes(wl, out_bytes=2, window_left=-1):
     """Algorithmic bytes of one step: attention reads each sequence's N_s K
     and V rows once per KV head plus Q and writes O; the append reads the new
     K/V rows and writes them into the caches; the slot step and the tables
-    are listed separately."""
+    are listed separately.  With a sliding window a decoding row needs only
+    the last window_left + 1 keys."""
     eb = {"f32": 4, "bf16": 2, "e4m3": 1}[wl.kv]
     sb = 4 if wl.src == "f32" else 2
     kv = wl.kv_bytes_read()
+    if window_left >= 0:
+        if int(wl.q_lens.max()) > 1:
+            raise ValueError("window byte accounting is for decode workloads")
+        n = wl.seq_lens[wl.q_lens > 0].astype(np.int64)
+        kv = int(np.minimum(n, window_left + 1).sum()) * wl.Hkv * wl.D * eb * 2
     q = wl.T * wl.Hq * wl.D * sb
     o = wl.T * wl.Hq * wl.D * out_bytes
     app = wl.T * wl.Hkv * wl.D * 2 * (sb + eb)
@@ -228,11 +234,12 @@ def run_ours(args, rank, world):
     LAYERS = args.layers
     wl = make_workload(args.workload, rank)
     max_q = int(wl.q_lens.max())
-    ds = harness.DeviceStep(wl, device=dev, out_dtype=torch.bfloat16, layers=LAYERS, max_q_len=max_q)
+    ds = harness.DeviceStep(wl, device=dev, out_dtype=torch.bfloat16, layers=LAYERS, max_q_len=max_q,
+                            soft_cap=args.soft_cap, window_left=args.window_left)
     torch.cuda.synchronize()
     if pkv_device_errors(dev) != 0:
         raise RuntimeError("device error flags set during set-up")
-    nb = step_bytes(wl)
+    nb = step_bytes(wl, window_left=args.window_left)
     stream = torch.cuda.current_stream(dev)
 
     for i in range(args.warmup):
@@ -257,7 +264,7 @@ def run_ours(args, rank, world):
             pkv_append(ds.k_new, ds.v_new, ds.slots, kc, vc, wl.k_scale, wl.v_scale)
             e1.record(stream)
             pkv_attention(ds.q, ds.cu_q, ds.seq_lens, ds.bt, kc, vc, wl.scale, ds.out, wl.k_scale,
-                          wl.v_scale, max_q, ds.ws)
+                          wl.v_scale, max_q, ds.ws, soft_cap=args.soft_cap, window_left=args.window_left)
             e2.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -292,7 +299,9 @@ def run_ours(args, rank, world):
                    "step": "slot mapping + append + attention (one layer)",
                    "l2": f"inputs larger than L2: {LAYERS} layer cache(s) rotated, "
                          f"{nb['kv'] / 1e6:.0f} MB of live KV each",
-                   "bytes_per_step": nb, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "bytes_per_step": nb, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   **({"variant": {"soft_cap": args.soft_cap, "window_left": args.window_left}}
+                      if args.soft_cap > 0 or args.window_left >= 0 else {})},
         "roofline": {"bound": "hbm", "kernel": "pkv_attention (plan + decode kernels)",
                      "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
@@ -372,7 +381,7 @@ def run_e2e(ds, wl, nb, args, dev, world, max_q):
         pkv_slot_mapping(dst["cu"], dst["sl"], dst["bt"], wl.block_size, out=ds.slots)
         pkv_append(dst["k"], dst["v"], ds.slots, kc, vc, wl.k_scale, wl.v_scale)
         pkv_attention(dst["q"], dst["cu"], dst["sl"], dst["bt"], kc, vc, wl.scale, ds.out, wl.k_scale,
-                      wl.v_scale, max_q, ds.ws)
+                      wl.v_scale, max_q, ds.ws, soft_cap=args.soft_cap, window_left=args.window_left)
         out_h.copy_(ds.out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -528,6 +537,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=4, help="layer caches rotated across steps")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soft-cap", type=float, default=0.0, help="logits soft cap (variant; 0: off)")
+    ap.add_argument("--window-left", type=int, default=-1, help="sliding window (variant; < 0: off)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

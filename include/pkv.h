@@ -214,6 +214,35 @@ PKV_API pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqle
                          float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pkv_attention_ex -- pkv_attention with two of the variants a kernel
+ * family is built for ("How Easy Is It to Start Serving LLMs?", "2. JIT
+ * compilation: one template, a kernel per variant": logit soft-capping and
+ * sliding windows).
+ *
+ *   logits_soft_cap  > 0: every scaled score s = scale * q.k becomes
+ *                    logits_soft_cap * tanh(s / logits_soft_cap) before the
+ *                    softmax; 0 turns it off.  Must be finite.
+ *   window_left      >= 0: the query at position p attends to keys
+ *                    max(0, p - window_left) .. p; < 0 turns it off.
+ *
+ * Built for decode rows (bf16 and e4m3 caches) and for prefill rows on bf16
+ * caches whose block size is a multiple of 16; other cases return
+ * PKV_ERR_UNSUPPORTED.  variant == NULL is pkv_attention.  With a window, a
+ * decode reads only the blocks its window touches.
+ */
+typedef struct {
+  float logits_soft_cap;
+  int32_t window_left;
+} pkv_attention_variant;
+
+PKV_API pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
+                                    const pkv_tensor* seq_lens, const pkv_tensor* block_tables,
+                                    const pkv_tensor* k_cache, const pkv_tensor* v_cache, float scale,
+                                    float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                                    const pkv_attention_variant* variant, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
 /* Size of the scratch array inside the library that
  * pkv_attention_static_workspace uses on each device (16 MiB). */
 #define PKV_STATIC_WORKSPACE_BYTES (16u << 20)

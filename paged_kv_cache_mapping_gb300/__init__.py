@@ -27,7 +27,7 @@ __all__ = ["PkvError", "pkv_slot_mapping", "pkv_csr_to_block_tables", "pkv_appen
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpkv.so")
-EXPORTED = ("pkv_slot_mapping", "pkv_append", "pkv_attention_workspace_size", "pkv_attention",
+EXPORTED = ("pkv_slot_mapping", "pkv_append", "pkv_attention_workspace_size", "pkv_attention", "pkv_attention_ex",
             "pkv_attention_static_workspace", "pkv_device_errors", "pkv_status_string", "pkv_last_error",
             "pkv_version", "pkv_csr_to_block_tables", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_append",
             "pkv_bm_free_sequence", "pkv_bm_block_table", "pkv_bm_build_step", "pkv_bm_stats")
@@ -46,6 +46,10 @@ class PkvError(RuntimeError):
 class _Tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class _Variant(ctypes.Structure):
+    _fields_ = [("logits_soft_cap", ctypes.c_float), ("window_left", ctypes.c_int32)]
 
 
 _lib = None
@@ -76,6 +80,10 @@ def load_library():
         lib.pkv_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_int32, P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         lib.pkv_attention.restype = st
+        lib.pkv_attention_ex.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                         ctypes.c_int32, P, ctypes.POINTER(_Variant), ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p]
+        lib.pkv_attention_ex.restype = st
         lib.pkv_attention_static_workspace.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float,
                                                        ctypes.c_float, ctypes.c_int32, P, ctypes.c_void_p]
         lib.pkv_attention_static_workspace.restype = st
@@ -168,8 +176,10 @@ def pkv_attention_workspace_size(q, block_tables, k_cache) -> int:
 
 
 def pkv_attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale: float, out,
-                  k_scale: float = 1.0, v_scale: float = 1.0, max_q_len: int = 0, workspace=None):
-    """Causal GQA attention of q [T, Hq, D] over the paged caches into out."""
+                  k_scale: float = 1.0, v_scale: float = 1.0, max_q_len: int = 0, workspace=None,
+                  soft_cap: float = 0.0, window_left: int = -1):
+    """Causal GQA attention of q [T, Hq, D] over the paged caches into out.
+    soft_cap > 0 or window_left >= 0 select the variants (pkv_attention_ex)."""
     lib = load_library()
     if workspace is None:
         workspace = torch.empty(pkv_attention_workspace_size(q, block_tables, k_cache), dtype=torch.uint8,
@@ -178,11 +188,16 @@ def pkv_attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, sca
         _tensor(q, "q"), _tensor(cu_seqlens_q, "cu_seqlens_q"), _tensor(seq_lens, "seq_lens"),
         _tensor(block_tables, "block_tables"), _tensor(k_cache, "k_cache"), _tensor(v_cache, "v_cache"),
         _tensor(out, "out"))
-    _check(lib.pkv_attention(ctypes.byref(tq), ctypes.byref(tcu), ctypes.byref(tsl), ctypes.byref(tbt),
-                             ctypes.byref(tkc), ctypes.byref(tvc), float(scale), float(k_scale),
-                             float(v_scale), int(max_q_len), ctypes.byref(to),
-                             ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
-                             _stream(q.device)))
+    ws = (ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(), _stream(q.device))
+    if soft_cap > 0 or window_left >= 0:
+        var = _Variant(float(soft_cap), int(window_left))
+        _check(lib.pkv_attention_ex(ctypes.byref(tq), ctypes.byref(tcu), ctypes.byref(tsl), ctypes.byref(tbt),
+                                    ctypes.byref(tkc), ctypes.byref(tvc), float(scale), float(k_scale),
+                                    float(v_scale), int(max_q_len), ctypes.byref(to), ctypes.byref(var), *ws))
+    else:
+        _check(lib.pkv_attention(ctypes.byref(tq), ctypes.byref(tcu), ctypes.byref(tsl), ctypes.byref(tbt),
+                                 ctypes.byref(tkc), ctypes.byref(tvc), float(scale), float(k_scale),
+                                 float(v_scale), int(max_q_len), ctypes.byref(to), *ws))
     return out
 
 

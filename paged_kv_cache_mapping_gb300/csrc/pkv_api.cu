@@ -5,6 +5,7 @@
 // outputs and the attention workspace.  Its one piece of static device
 // state is the error word below, which the kernels OR bits into when they
 // meet an out-of-range index instead of faulting.
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -420,10 +421,15 @@ pkv_status pkv_attention_workspace_size(const pkv_tensor* q, const pkv_tensor* b
   return PKV_OK;
 }
 
-pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
-                         const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
-                         float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                          const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                          float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                          float soft_cap, int32_t window_left, void* workspace, size_t workspace_bytes,
+                          void* stream) {
   PKV_TRY(check_tensor("q", q, 3));
   PKV_TRY(check_tensor("out", out, 3));
   PKV_TRY(check_tensor("seq_lens", seq_lens, 1));
@@ -508,12 +514,18 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
   p.D = static_cast<int32_t>(D);
   const float kLog2e = 1.4426950408889634f;
   p.qk_scale_log2 = scale * (kv == 2 ? k_scale : 1.0f) * kLog2e;
+  p.soft_cap = soft_cap > 0.f ? soft_cap : 0.f;
+  p.cap_pre = p.soft_cap > 0.f ? scale * (kv == 2 ? k_scale : 1.0f) / soft_cap : 0.f;
+  p.cap_post = p.soft_cap > 0.f ? soft_cap * kLog2e : 0.f;
+  p.window_left = window_left >= 0 ? window_left : -1;
   p.v_scale = kv == 2 ? v_scale : 1.0f;
   p.decode_max_g = 8;
   p.err = err;
   const int out_kind = out->dtype == PKV_BF16 ? 1 : 0;
   cudaError_t e;
   if (kv == 0) {
+    if (p.soft_cap > 0.f || p.window_left >= 0)
+      return fail(PKV_ERR_UNSUPPORTED, "a soft cap or sliding window is built for bf16 and e4m3 caches");
     e = pkv::launch_f32(p, out_kind, T, st);
     if (e != cudaSuccess) return cuda_fail(e, "f32 attention launch");
     return finish(st, "pkv_attention");
@@ -537,6 +549,10 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
   const int G = p.G;
   const bool prefill = (max_q_len > 1) || (max_q_len <= 0 && T >= 2) || G > p.decode_max_g;
   const bool tc = prefill && pkv::prefill_tc_supported(kv, D, bs, G);
+  const bool variant = p.soft_cap > 0.f || p.window_left >= 0;
+  if (variant && prefill && !tc)
+    return fail(PKV_ERR_UNSUPPORTED, "a soft cap or sliding window needs decode rows, or prefill rows on bf16 "
+                                     "caches with block sizes a multiple of 16 (max_q_len > 1 here)");
   p.pf_tq = tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
   e = pkv::launch_plan(p, st);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
@@ -554,6 +570,35 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return finish(st, "pkv_attention");
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                         const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                         float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return attention_impl(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale,
+                        max_q_len, out, 0.f, -1, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                            const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                            float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                            const pkv_attention_variant* variant, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  float cap = 0.f;
+  int32_t window = -1;
+  if (variant != nullptr) {
+    PKV_TRY(need(variant->logits_soft_cap >= 0.f && variant->logits_soft_cap < INFINITY,
+                 "logits_soft_cap must be finite and >= 0 (0: off)"));
+    cap = variant->logits_soft_cap;
+    window = variant->window_left < 0 ? -1 : variant->window_left;
+  }
+  return attention_impl(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale,
+                        max_q_len, out, cap, window, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

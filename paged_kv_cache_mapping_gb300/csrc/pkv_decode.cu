@@ -87,6 +87,11 @@ __device__ __forceinline__ void block_scan(const int (&v)[K], int (&off)[K], int
   }
 }
 
+// First key a decoding query (position n - 1) sees.
+__device__ __forceinline__ int decode_first_key(const AttnParams& p, int n) {
+  return p.window_left >= 0 && n - 1 - p.window_left > 0 ? n - 1 - p.window_left : 0;
+}
+
 // Work counts of sequence s: decode chunks (all, full, ragged last) or
 // prefill tiles.  Inconsistent lengths give no work (and are recorded).
 struct SeqCounts {
@@ -104,9 +109,11 @@ __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool
     return c;
   }
   if (q_s == 1 && p.G <= p.decode_max_g) {
-    const int k = chunk_shift(n);
-    c.dec = (int)(((unsigned)n + (1u << k) - 1u) >> k);
-    c.full = n >> k;
+    // the visible keys [lo, n) are cut into chunks of 2^k from lo
+    const int lo = decode_first_key(p, n);
+    const int k = chunk_shift(n - lo);
+    c.dec = (int)(((unsigned)(n - lo) + (1u << k) - 1u) >> k);
+    c.full = (n - lo) >> k;
     c.tail = c.dec - c.full;
   } else {
     c.pf = p.pf_tq > 0 ? (q_s + p.pf_tq - 1) / p.pf_tq
@@ -152,9 +159,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
       const int n = __ldg(p.seq_lens + s);
       const int t0 = __ldg(p.cu_q + s);
       if (c.dec > 0) {
-        const int k = chunk_shift(n);
+        const int first = decode_first_key(p, n);
+        const int k = chunk_shift(n - first);
         for (int ch = 0; ch < c.dec; ++ch) {
-          const int k0 = ch << k;
+          const int k0 = first + (ch << k);
           const int4 lo = make_int4(s, k0, min(k0 + (1 << k), n), t0);
           const int4 hi = make_int4(c.dec, off[0], ch, 0);
           const int slot = ch < c.full ? off[1] + ch : tot[1] + off[2];
@@ -736,10 +744,17 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
       // the tokens of accumulator rows g4 and g4 + 8
       const int tr0 = KV == 2 ? 2 * g4 : g4, tr1 = KV == 2 ? 2 * g4 + 1 : g4 + 8;
       const bool v0 = j0 + tr0 < k1, v1 = j0 + tr1 < k1;
-      const float x0 = v0 ? sc[0] * p.qk_scale_log2 : -INFINITY;
-      const float x1 = v0 ? sc[1] * p.qk_scale_log2 : -INFINITY;
-      const float x2 = v1 ? sc[2] * p.qk_scale_log2 : -INFINITY;
-      const float x3 = v1 ? sc[3] * p.qk_scale_log2 : -INFINITY;
+      if (p.soft_cap > 0.f) {  // soft cap: cap * tanh(s / cap), in base 2
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = p.cap_post * tanhf(sc[e] * p.cap_pre);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] *= p.qk_scale_log2;
+      }
+      const float x0 = v0 ? sc[0] : -INFINITY;
+      const float x1 = v0 ? sc[1] : -INFINITY;
+      const float x2 = v1 ? sc[2] : -INFINITY;
+      const float x3 = v1 ? sc[3] : -INFINITY;
       float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
       mx0 = warp_max_xor(mx0, 4); mx0 = warp_max_xor(mx0, 8); mx0 = warp_max_xor(mx0, 16);
       mx1 = warp_max_xor(mx1, 4); mx1 = warp_max_xor(mx1, 8); mx1 = warp_max_xor(mx1, 16);

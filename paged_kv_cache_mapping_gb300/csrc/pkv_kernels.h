@@ -105,6 +105,12 @@ struct AttnParams {
   int32_t hp;            // decode: KV heads per work item (consumer warps), divides Hkv, <= 8
   int32_t ns;            // decode: stages in the staging ring
   int32_t pf_tq;         // tensor-core prefill: query tokens per tile (0: the mma.sync prefill tiles)
+  // variants: soft_cap > 0 turns a score s into soft_cap * tanh(s / soft_cap);
+  // the kernels take x = cap_post * tanh(raw * cap_pre) in base 2, raw being
+  // the q.k dot product of the stored values.  window_left >= 0: the query
+  // at position p sees keys p - window_left .. p.
+  float soft_cap, cap_pre, cap_post;
+  int32_t window_left;
   Workspace ws;
   unsigned int* err;
 };

@@ -227,19 +227,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_units = p.ws.pf_off[p.B] * Hkv;
   const uint32_t q_box_bytes = (uint32_t)(Geo::kHalves * G * tq * 128);
 
+  // Key tiles of a unit: from the first tile any of its rows sees (a sliding
+  // window skips the ones before) to the tile of its last row's last key.
+  auto unit_tiles = [&](const PrefillDesc& e, int& kt0, int& n_kt) {
+    const int first = p.window_left >= 0 ? max(0, e.n - e.q_s + e.r0 - p.window_left) : 0;
+    kt0 = first / kTcKeys;
+    n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys - kt0;
+  };
   // K or V tiles of one unit, one TMA box (16 keys x one d half) per lane;
   // the block-table entry of the next tile is loaded while this one is issued
   auto stream_kv = [&](const PrefillDesc& e, int hk, int& g, bool is_v) -> bool {
     const int64_t n_slots = p.num_blocks * p.bs;
     const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
-    const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
+    int kt0, n_kt;
+    unit_tiles(e, kt0, n_kt);
     const int bi = lane & 3, h = (lane >> 2) & 1;  // keys 16 bi .. +15 of the tile, d half h
     const bool issuer = lane < 4 * Geo::kHalves;
     constexpr int32_t kPast = INT32_MIN;  // a block past the sequence
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
     const uint32_t base = is_v ? sV : sK;
     auto load_blk = [&](int kt) -> int32_t {
-      const int key0 = kt * kTcKeys + 16 * bi;
+      const int key0 = (kt0 + kt) * kTcKeys + 16 * bi;
       int32_t v = kPast;
       if (key0 < e.n) v = __ldg(bt_row + (p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs)));
       return v;
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int kt = 0; kt < n_kt; ++kt, ++g) {
       int32_t nxt = kPast;
       if (kt + 1 < n_kt) nxt = load_blk(kt + 1);
-      const int key0 = kt * kTcKeys + 16 * bi;
+      const int key0 = (kt0 + kt) * kTcKeys + 16 * bi;
       int slot = (int)n_slots;  // out of bounds: TMA fills zeros
       if ((uint32_t)blk < (uint32_t)p.num_blocks) {
         const int lb = p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs);
@@ -339,7 +347,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++ui;
       if (!ok || u >= n_units) break;
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
-      const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
+      int kt0, n_kt;
+      unit_tiles(e, kt0, n_kt);
       ok = mbar_wait_warp(q_full, q_it & 1, p.err);
       // S[g % 2] = Q K^T for key tile g
       auto issue_qk = [&](int gg) -> bool {
@@ -419,7 +428,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!ok || u >= n_units) break;
       const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int hk = u - (u / Hkv) * Hkv;
-      const int n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys;
+      int kt0, n_kt;
+      unit_tiles(e, kt0, n_kt);
       const int tok = r / G, hj = r - tok * G;
       const int i = e.r0 + tok;                          // query index in the sequence
       const bool valid = tok < tq && i < e.r1;
@@ -436,11 +446,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_ld32(tmem + sb * kTcKeys + lane_off, v0);
           tmem_ld32(tmem + sb * kTcKeys + lane_off + 32, v1);
           tmem_wait_ld();
-          const int lim = valid ? pos - t * kTcKeys : -1;  // columns 0 .. lim are visible
+          // columns lo_c .. lim are visible (lo_c <= 0 without a window)
+          const int kbase = (kt0 + t) * kTcKeys;
+          const int lim = valid ? pos - kbase : -1;
+          const int lo_c = p.window_left >= 0 ? pos - p.window_left - kbase : INT32_MIN;
+          if (p.soft_cap > 0.f) {  // soft cap: cap * tanh(s / cap), in base 2
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            x[c] = c <= lim ? __uint_as_float(v0[c]) * p.qk_scale_log2 : -INFINITY;
-            x[c + 32] = c + 32 <= lim ? __uint_as_float(v1[c]) * p.qk_scale_log2 : -INFINITY;
+            for (int c = 0; c < 32; ++c) {
+              x[c] = c <= lim && c >= lo_c ? p.cap_post * tanhf(__uint_as_float(v0[c]) * p.cap_pre) : -INFINITY;
+              x[c + 32] = c + 32 <= lim && c + 32 >= lo_c ? p.cap_post * tanhf(__uint_as_float(v1[c]) * p.cap_pre)
+                                                          : -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              x[c] = c <= lim && c >= lo_c ? __uint_as_float(v0[c]) * p.qk_scale_log2 : -INFINITY;
+              x[c + 32] = c + 32 <= lim && c + 32 >= lo_c ? __uint_as_float(v1[c]) * p.qk_scale_log2 : -INFINITY;
+            }
           }
         }
         tc_fence_before();

@@ -41,8 +41,10 @@ class DeviceStep:
     """
 
     def __init__(self, wl: Workload, device="cuda", out_dtype=torch.float32, layers: int = 1,
-                 max_q_len: int = None, slot_dtype=torch.int32, history_batch: int = 1 << 21):
+                 max_q_len: int = None, slot_dtype=torch.int32, history_batch: int = 1 << 21,
+                 soft_cap: float = 0.0, window_left: int = -1):
         self.wl = wl
+        self.soft_cap, self.window_left = soft_cap, window_left
         self.device = torch.device(device)
         dev = self.device
         self.bt = torch.from_numpy(np.ascontiguousarray(wl.block_tables, np.int32)).to(dev)
@@ -82,12 +84,14 @@ class DeviceStep:
         pkv_slot_mapping(self.cu_q, self.seq_lens, self.bt, wl.block_size, out=self.slots)
         pkv_append(self.k_new, self.v_new, self.slots, kc, vc, wl.k_scale, wl.v_scale)
         pkv_attention(self.q, self.cu_q, self.seq_lens, self.bt, kc, vc, wl.scale,
-                      self.out if out is None else out, wl.k_scale, wl.v_scale, self.max_q_len, self.ws)
+                      self.out if out is None else out, wl.k_scale, wl.v_scale, self.max_q_len, self.ws,
+                      soft_cap=self.soft_cap, window_left=self.window_left)
         return self.out if out is None else out
 
     def attention_only(self, layer: int = 0, out=None):
         wl = self.wl
         kc, vc = self.caches[layer]
         pkv_attention(self.q, self.cu_q, self.seq_lens, self.bt, kc, vc, wl.scale,
-                      self.out if out is None else out, wl.k_scale, wl.v_scale, self.max_q_len, self.ws)
+                      self.out if out is None else out, wl.k_scale, wl.v_scale, self.max_q_len, self.ws,
+                      soft_cap=self.soft_cap, window_left=self.window_left)
         return self.out if out is None else out
