@@ -6,26 +6,37 @@
 // tokens of a prefill chunk attend causally over the cached prefix and the
 // chunk itself, in the same packed step as the decodes.  A tile of 128 query
 // rows (whole tokens x the G query heads of one KV head) against a tile of
-// 64 keys is a dense contraction, run here as
-//     S = Q K^T      (M 128, N 64 keys, K = D; bf16 in, fp32 in TMEM)
-//     O += P V       (M 128, N = D, K 64 keys; P split into bf16 hi + lo)
+// 128 keys is a dense contraction, run here as
+//     S = Q K^T      (M 128, N 128 keys, K = D; bf16 in, fp32 in TMEM)
+//     O += P V       (M 128, N = D, K 128 keys; P split into bf16 hi + lo)
 // with an online softmax (base 2) between them, one thread per query row.
+// P never leaves tensor memory: each softmax thread overwrites its row of S
+// with the hi and lo bf16 parts of P (64 packed columns each) and the P V
+// MMAs read their A operand from there.  An M 128 x N 128 x K 16 MMA keeps
+// the tensor core at its full rate; N 64 would run at about two thirds.
 //
-// CTA (one per SM, persistent over tiles), 7 warps:
+// CTA (one per SM, persistent over tiles), 11 warps:
 //   warp 0   TMA producer: claims work units, loads the Q tile of each and
-//            its K tiles of 64 keys (4 boxes of 16 consecutive slots of one
-//            head per d half) into a 3-stage ring.
-//   warp 6   TMA producer of the V tiles, in its own 3-stage ring.
+//            its K tiles of 128 keys (8 boxes of 16 consecutive slots of one
+//            head per d half) into a 2-stage ring.
+//   warp 2   TMA producer of the V tiles, in its own 3-stage ring.
 //            Keys past the sequence and bad block ids read out of bounds,
 //            which TMA fills with zeros.
 //   warp 1   MMA issuer (one thread) and owner of the TMEM allocation
-//            (S double-buffered in columns 0-127, O in columns 128-127+D).
-//   warps 2-5  softmax: each thread loads its row of S from TMEM, masks it,
-//            writes its row of P (hi and lo bf16 parts) into one of two
-//            shared P buffers and, only when the row's max grows by more than
-//            2^8, waits for the previous P V and rescales its row of O in
-//            TMEM; at the end it writes O / l.  QK^T of the next tile and P V
-//            of the previous one run on the tensor core meanwhile.
+//            (S / P double-buffered in columns 0-255, O in 256-255+D).
+//            MMAs issued by one thread run in issue order, so the Q K^T that
+//            overwrites an S buffer is issued after the P V that reads it.
+//   warps 3-10  softmax, two threads per query row (a warp may only reach
+//            the TMEM lanes of its quarter, so warps w and w + 4 share rows;
+//            the first takes keys 0-63 of each tile, the second 64-127).
+//            Each thread loads its half row of S from TMEM, masks it (only
+//            on tiles that cut a row's visible range), trades its partial
+//            max with its partner through shared memory, writes its half of
+//            P in place and, only when the row's max grows by more than 2^8,
+//            waits for the previous P V and rescales its half of the row of
+//            O in TMEM; at the end the partners add their sums and each
+//            writes half of O / l.  Q K^T of the next tile and P V of the
+//            previous one run on the tensor core meanwhile.
 // Block sizes must be multiples of 16 (a box of 16 keys lies in one block).
 #include <cuda.h>
 
@@ -37,9 +48,11 @@ namespace pkv {
 namespace {
 
 constexpr int kTcRows = 128;    // query rows per tile (MMA M)
-constexpr int kTcKeys = 64;     // keys per key tile
-constexpr int kTcStages = 3;    // K and V ring depth
-constexpr int kTcThreads = 224;  // 7 warps
+constexpr int kTcKeys = 128;    // keys per key tile (MMA N of Q K^T, K of P V)
+constexpr int kKStages = 2;     // K ring depth
+constexpr int kVStages = 3;     // V ring depth (V is read later than K: it is requested earlier)
+constexpr int kTcThreads = 352;  // 11 warps
+constexpr int kSoftmaxWarp0 = 3; // warps 3-10: two per TMEM lane quarter
 // A row's reference max moves only when a tile's max exceeds it by more than
 // this (log2 units), so p = 2^(x - m_ref) stays below 2^8 and O needs a
 // rescale in TMEM only then.
@@ -50,14 +63,16 @@ struct TcGeom {
   static constexpr int kHalves = D / 64;                     // 128-byte atoms along d
   static constexpr int kQBytes = kHalves * kTcRows * 128;
   static constexpr int kKVBytes = kHalves * kTcKeys * 128;   // one K or V tile
-  static constexpr int kPBytes = kTcRows * 128;              // one part (hi or lo) of a P tile: 64 keys
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kTcStages * kKVBytes;
-  static constexpr int kOffP = kOffV + kTcStages * kKVBytes; // [2 buffers][hi, lo]
-  static constexpr int kOffBar = kOffP + 4 * kPBytes;
-  static constexpr int kSmem = kOffBar + 512 + 1024;          // barriers, 1024-byte alignment slack
-  static constexpr uint32_t kTmemCols = 256;                  // S 2 x 64 columns, O D columns
+  static constexpr int kOffV = kOffK + kKStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
+  static constexpr int kOffX = kOffBar + 512;                 // row max / sum exchange [2][2][kTcRows]
+  static constexpr int kSmem = kOffX + 4 * kTcRows * 4 + 1024; // + 1024-byte alignment slack
+  static constexpr uint32_t kTmemCols = 512;                  // S / P 2 x 128 columns, O D columns
+  static constexpr uint32_t kColO = 2 * kTcKeys;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(kColO + D <= kTmemCols, "tensor memory");
 };
 
 // ---- tcgen05 / TMA wrappers
@@ -80,6 +95,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// the same with A read from tensor memory: row r of A in lane r, column c
+// holding elements 2c (low half) and 2c + 1 (high half) of the row
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -142,17 +167,10 @@ __device__ __forceinline__ void split_trunc_bf16(float p0, float p1, uint32_t& h
   lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
 
-// byte offset of element (row r, column c) in a K-major, 128-byte-swizzled
-// tile of `rows` rows of 16-bit elements (64 columns per atom)
-__device__ __forceinline__ uint32_t sw128_off(int r, int c, int rows) {
-  return (uint32_t)((c >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
-                    ((c & 7) << 1));
-}
-
 // Work unit u: prefill tile u / Hkv (tokens r0 .. r1-1 of its sequence,
 // the last tokens first), KV head u % Hkv.  Key tiles are numbered across
-// the CTA's units (g); tile g uses K/V stage g % 3, S buffer g % 2, P buffer
-// g % 2 and signals o_done[g % 2] when its P V has finished.
+// the CTA's units (g); tile g uses K/V stage g % 3 and S / P buffer g % 2,
+// and signals o_done[g % 2] when its P V has finished.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -163,8 +181,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sQ = smem_u32(smem + Geo::kOffQ);
   const uint32_t sK = smem_u32(smem + Geo::kOffK);
   const uint32_t sV = smem_u32(smem + Geo::kOffV);
-  const uint32_t sP = smem_u32(smem + Geo::kOffP);
-  unsigned char* pbase = smem + Geo::kOffP;
   const uint32_t b0 = smem_u32(smem + Geo::kOffBar);
   auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
   const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(22), drain = bar(23);
@@ -173,7 +189,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto v_full = [&](int s) { return bar(8 + s); };
   auto v_empty = [&](int s) { return bar(11 + s); };
   auto s_full = [&](int b) { return bar(14 + b); };
-  auto s_empty = [&](int b) { return bar(16 + b); };
   auto p_full = [&](int b) { return bar(18 + b); };
   auto o_done = [&](int b) { return bar(20 + b); };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * 24);
@@ -183,6 +198,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto unit_full = [&](int b) { return bar(26 + b); };
   auto unit_empty = [&](int b) { return bar(28 + b); };
   volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 30);
+  // the two softmax warps of TMEM lane quarter q trade per-row values
+  // through buffer b of xval, paired by barrier xbar(q, b)
+  auto xbar = [&](int q, int b) { return bar(32 + 2 * q + b); };
+  float* xval = reinterpret_cast<float*>(smem + Geo::kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the abort flag as one value for the whole warp (another warp may set it
   // between two lanes' reads)
@@ -190,23 +209,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(s_empty(b), 4);
-      mbar_init(p_full(b), 4);
+      mbar_init(p_full(b), 8);
       mbar_init(o_done(b), 1);
     }
-    mbar_init(o_free, 4);
+    mbar_init(o_free, 8);
     mbar_init(drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(unit_full(b), 1);
-      mbar_init(unit_empty(b), 6);  // the V producer, the MMA warp and the 4 softmax warps
+      mbar_init(unit_empty(b), 10);  // the V producer, the MMA warp and the 8 softmax warps
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(xbar(q, 0), 2);
+      mbar_init(xbar(q, 1), 2);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -220,7 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tO = tmem + 2 * kTcKeys;  // S buffers: columns 0 .. 2 * kTcKeys - 1
+  const uint32_t tO = tmem + Geo::kColO;  // S / P buffers: columns 0 .. 2 * kTcKeys - 1
 
   const int G = p.G, Hkv = p.Hkv;
   const int tq = p.pf_tq;  // query tokens per tile
@@ -241,8 +265,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
     int kt0, n_kt;
     unit_tiles(e, kt0, n_kt);
-    const int bi = lane & 3, h = (lane >> 2) & 1;  // keys 16 bi .. +15 of the tile, d half h
-    const bool issuer = lane < 4 * Geo::kHalves;
+    const int bi = lane & 7, h = (lane >> 3) & 1;  // keys 16 bi .. +15 of the tile, d half h
+    const bool issuer = lane < 8 * Geo::kHalves;
     constexpr int32_t kPast = INT32_MIN;  // a block past the sequence
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
     const uint32_t base = is_v ? sV : sK;
@@ -264,7 +288,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else if (blk != kPast) {
         atomicOr(p.err, kErrBlockRange);
       }
-      const int st = g % kTcStages, ph = (g / kTcStages) & 1;
+      const int ns = is_v ? kVStages : kKStages;
+      const int st = g % ns, ph = (g / ns) & 1;
       const uint32_t full = is_v ? v_full(st) : k_full(st), empty = is_v ? v_empty(st) : k_empty(st);
       if (!mbar_wait_warp(empty, ph ^ 1, p.err)) return false;
       if (lane == 0) mbar_arrive_expect_tx(full, Geo::kKVBytes);
@@ -276,8 +301,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
   // giving up: let the copies a producer warp issued land before the CTA exits
   auto drain_copies = [&](int g, bool is_v) {
-    for (int k = g - 1; k >= 0 && k >= g - kTcStages; --k)
-      mbar_wait_warp(is_v ? v_full(k % kTcStages) : k_full(k % kTcStages), (k / kTcStages) & 1, p.err);
+    const int ns = is_v ? kVStages : kKStages;
+    for (int k = g - 1; k >= 0 && k >= g - ns; --k)
+      mbar_wait_warp(is_v ? v_full(k % ns) : k_full(k % ns), (k / ns) & 1, p.err);
   };
 
   if (warp == 0) {
@@ -315,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       u = __shfl_sync(0xffffffffu, claim, 0);
     }
     if (aborted()) drain_copies(g, false);
-  } else if (warp == 6) {
+  } else if (warp == 2) {
     // ======================= TMA producer: V =======================
     // runs on its own so that K tiles are not held back by the V ring
     int g = 0, ui = 0;
@@ -352,9 +378,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = mbar_wait_warp(q_full, q_it & 1, p.err);
       // S[g % 2] = Q K^T for key tile g
       auto issue_qk = [&](int gg) -> bool {
-        const int st = gg % kTcStages, ph = (gg / kTcStages) & 1, sb = gg & 1;
+        const int st = gg % kKStages, ph = (gg / kKStages) & 1, sb = gg & 1;
+        // S buffer sb last held P of tile gg - 2, whose P V was issued before
+        // this Q K^T (issue order is execution order)
         if (!mbar_wait_warp(k_full(st), ph, p.err)) return false;
-        if (!mbar_wait_warp(s_empty(sb), ((gg >> 1) & 1) ^ 1, p.err)) return false;
         tc_fence_after();
         if (lane == 0) {
           // a descriptor's start address is its low field (bytes >> 4): the
@@ -381,19 +408,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           umma_commit(q_empty);  // the unit's Q is no longer read
         }
         if (!ok) break;
-        const int st = gg % kTcStages, ph = (gg / kTcStages) & 1, pb = gg & 1;
+        const int st = gg % kVStages, ph = (gg / kVStages) & 1, pb = gg & 1;
         ok = mbar_wait_warp(p_full(pb), (gg >> 1) & 1, p.err) && mbar_wait_warp(v_full(st), ph, p.err) &&
              (t > 0 || mbar_wait_warp(o_free, (q_it & 1) ^ 1, p.err));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint64_t dp = umma_desc(sP + pb * 2 * Geo::kPBytes, 16, 1024);
+          // P hi in columns 0-63 of the buffer, P lo in 64-127: 16 keys are
+          // 8 columns; V is MN-major, 16 keys = 2048 bytes of each d half
+          const uint32_t tp = tmem + pb * kTcKeys;
           const uint64_t dv = umma_desc(sV + st * Geo::kKVBytes, kTcKeys * 128, 1024);
           const uint32_t acc0 = t > 0;
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            umma_bf16(tO, dp + kk * 2, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);  // P hi
-            umma_bf16(tO, dp + (Geo::kPBytes >> 4) + kk * 2, dv + kk * 128, kIdPV, 1);  // P lo
+            umma_bf16_ta(tO, tp + kk * 8, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);                // P hi
+            umma_bf16_ta(tO, tp + kTcKeys / 2 + kk * 8, dv + kk * 128, kIdPV, 1);                  // P lo
           }
           umma_commit(o_done(pb));
           umma_commit(v_empty(st));
@@ -410,12 +439,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait_warp(drain, 0, p.err);
     }
   } else {
-    // ======================= softmax / epilogue (warps 2-5) =======================
-    const int quarter = warp & 3;             // TMEM lanes 32 * quarter ..
-    const int r = 32 * quarter + lane;        // this thread's query row
+    // ======================= softmax / epilogue (warps 3-10) =======================
+    const int quarter = warp & 3;                        // TMEM lanes 32 * quarter ..
+    const int half = (warp - kSoftmaxWarp0) >> 2;        // keys 64 half .. of each tile
+    const int r = 32 * quarter + lane;                   // this thread's query row
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    int g = 0, ui = 0;
+    constexpr int kHalfKeys = kTcKeys / 2;
+    constexpr int kHalfD = D / 2;
+    int g = 0, ui = 0, xj = 0;
     bool ok = true;
+    // gives this thread's value for its row to the partner thread and
+    // returns the partner's (double-buffered; the partner makes the same
+    // sequence of calls)
+    auto trade = [&](float mine, float& theirs) -> bool {
+      const int b = xj & 1;
+      const uint32_t par = (uint32_t)(xj >> 1) & 1u;
+      ++xj;
+      xval[(b * 2 + half) * kTcRows + r] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar(quarter, b));
+      if (!mbar_wait_warp(xbar(quarter, b), par, p.err)) return false;
+      theirs = xval[(b * 2 + (half ^ 1)) * kTcRows + r];
+      return true;
+    };
     while (ok && !aborted()) {
       int u = n_units;
       ok = mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err);
@@ -434,61 +480,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int i = e.r0 + tok;                          // query index in the sequence
       const bool valid = tok < tq && i < e.r1;
       const int pos = e.n - e.q_s + i;                   // absolute position: keys 0 .. pos
-      float m = -INFINITY, l = 0.f;                      // reference max (base 2), sum
+      float m = -INFINITY, l = 0.f;                      // reference max (base 2), this half's sum
       for (int t = 0; t < n_kt; ++t) {
         const int gg = g + t, sb = gg & 1;
+        const uint32_t ts = tmem + sb * kTcKeys + lane_off;  // this row of S, then of P
         if (!mbar_wait_warp(s_full(sb), (gg >> 1) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
-        // S row into registers, scaled and masked
-        float x[kTcKeys];
+        float x[kHalfKeys];  // this half row of S; x * xs is the base-2 logit
         {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(tmem + sb * kTcKeys + lane_off, v0);
-          tmem_ld32(tmem + sb * kTcKeys + lane_off + 32, v1);
+          uint32_t u0[32], u1[32];
+          tmem_ld32(ts + kHalfKeys * half, u0);
+          tmem_ld32(ts + kHalfKeys * half + 32, u1);
           tmem_wait_ld();
-          // columns lo_c .. lim are visible (lo_c <= 0 without a window)
-          const int kbase = (kt0 + t) * kTcKeys;
-          const int lim = valid ? pos - kbase : -1;
-          const int lo_c = p.window_left >= 0 ? pos - p.window_left - kbase : INT32_MIN;
-          if (p.soft_cap > 0.f) {  // soft cap: cap * tanh(s / cap), in base 2
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              x[c] = c <= lim && c >= lo_c ? p.cap_post * tanhf(__uint_as_float(v0[c]) * p.cap_pre) : -INFINITY;
-              x[c + 32] = c + 32 <= lim && c + 32 >= lo_c ? p.cap_post * tanhf(__uint_as_float(v1[c]) * p.cap_pre)
-                                                          : -INFINITY;
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              x[c] = c <= lim && c >= lo_c ? __uint_as_float(v0[c]) * p.qk_scale_log2 : -INFINITY;
-              x[c + 32] = c + 32 <= lim && c + 32 >= lo_c ? __uint_as_float(v1[c]) * p.qk_scale_log2 : -INFINITY;
-            }
+          for (int j = 0; j < 32; ++j) {
+            x[j] = __uint_as_float(u0[j]);
+            x[32 + j] = __uint_as_float(u1[j]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty(sb));
+        // with a positive scale the max is taken on the raw scores and the
+        // scale folds into the exponent's FMA; a soft cap (or another scale)
+        // turns the row into logits first
+        const bool raw_max = p.soft_cap <= 0.f && p.qk_scale_log2 > 0.f;
+        const float xs = raw_max ? p.qk_scale_log2 : 1.f;
+        if (!raw_max) {
+          if (p.soft_cap > 0.f) {  // soft cap: cap * tanh(s / cap), in base 2
+#pragma unroll
+            for (int c = 0; c < kHalfKeys; ++c) x[c] = p.cap_post * tanhf(x[c] * p.cap_pre);
+          } else {
+#pragma unroll
+            for (int c = 0; c < kHalfKeys; ++c) x[c] *= p.qk_scale_log2;
+          }
+        }
+        {  // columns lo_c .. lim of this half are visible (lo_c <= 0 without
+           // a window); a half tile inside every row's visible range needs no mask
+          const int kbase = (kt0 + t) * kTcKeys + kHalfKeys * half;
+          const int lim = valid ? pos - kbase : -1;
+          const int lo_c = p.window_left >= 0 ? pos - p.window_left - kbase : INT32_MIN;
+          if (__any_sync(0xffffffffu, lim < kHalfKeys - 1 || lo_c > 0)) {
+#pragma unroll
+            for (int c = 0; c < kHalfKeys; ++c) x[c] = c <= lim && c >= lo_c ? x[c] : -INFINITY;
+          }
+        }
         float mx;
-        {  // tree reduction: the row is one warp lane's, so no shuffles
+        {  // tree reduction over this half, then the partner's half
           float t8[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) t8[j] = x[j];
 #pragma unroll
-          for (int c = 8; c < kTcKeys; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
+          for (int c = 8; c < kHalfKeys; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
           mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+          float other;
+          if (!trade(mx, other)) { ok = false; break; }
+          mx = fmaxf(mx, other) * xs;
         }
-        // move the reference max only when this tile exceeds it by more than tau
+        // move the reference max only when this tile exceeds it by more than
+        // tau (both partners see the same mx, m and so decide alike)
         const bool need = mx > m + kTcTau;
         if (__any_sync(0xffffffffu, need)) {
           const float mn = need ? mx : m;
           const float alpha = mn == -INFINITY ? 1.f : ex2_approx(m - mn);
           if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
             // O holds every P V of the unit so far: wait for the last, rescale
+            // this thread's half of the row
             const int pg = gg - 1;
             if (!mbar_wait_warp(o_done(pg & 1), (pg >> 1) & 1, p.err)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
+            for (int c = kHalfD * half; c < kHalfD * (half + 1); c += 32) {
               uint32_t v[32];
               tmem_ld32(tO + lane_off + c, v);
               tmem_wait_ld();
@@ -501,42 +560,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           l *= alpha;
           m = mn;
         }
-        // P buffer gg % 2 was last read by the P V of tile gg - 2
-        if (gg >= 2) {
-          const int pg = gg - 2;
-          if (!mbar_wait_warp(o_done(pg & 1), (pg >> 1) & 1, p.err)) { ok = false; break; }
-        }
+        // P = 2^(x - m) over the S columns the tile came from: hi parts of
+        // keys 2c, 2c + 1 in column c, lo parts 64 columns further.  The P V
+        // of tile gg - 2 that read this buffer finished before its Q K^T ran.
         const float ms = m == -INFINITY ? 0.f : m;
-        unsigned char* pdst = pbase + (gg & 1) * 2 * Geo::kPBytes;
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums, kept apart for latency
+        {
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums, kept apart for latency
+          uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int c = 0; c < kTcKeys; c += 8) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float p0 = ex2_approx(x[c + 2 * j] - ms), p1 = ex2_approx(x[c + 2 * j + 1] - ms);
-            s4[j] += p0 + p1;
-            split_trunc_bf16(p0, p1, hi[j], lo[j]);
+          for (int w = 0; w < 32; ++w) {
+            const float p0 = ex2_approx(fmaf(x[2 * w], xs, -ms));
+            const float p1 = ex2_approx(fmaf(x[2 * w + 1], xs, -ms));
+            s4[w & 3] += p0 + p1;
+            split_trunc_bf16(p0, p1, hi[w], lo[w]);
           }
-          const uint32_t off = sw128_off(r, c, kTcRows);
-          *reinterpret_cast<uint4*>(pdst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(pdst + Geo::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          tmem_st32(ts + 32 * half, hi);
+          tmem_st32(ts + kHalfKeys + 32 * half, lo);
+          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
-        l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(gg & 1));
+        if (lane == 0) mbar_arrive(p_full(sb));
       }
       if (!ok) break;
-      // epilogue: O / l for valid rows, after the unit's last P V
+      // epilogue: O / l for valid rows, after the unit's last P V; the
+      // partners add their halves' sums and each writes half of the row
       const int lg = g + n_kt - 1;
       if (!mbar_wait_warp(o_done(lg & 1), (lg >> 1) & 1, p.err)) { ok = false; break; }
       tc_fence_after();
-      const float inv = valid && l > 0.f ? p.v_scale / l : 0.f;
+      float l_other;
+      if (!trade(l, l_other)) { ok = false; break; }
+      const float lt = l + l_other;
+      const float inv = valid && lt > 0.f ? p.v_scale / lt : 0.f;
       OutT* dst = static_cast<OutT*>(p.out) + (int64_t)(e.t0 + i) * p.o_st + (int64_t)(hk * G + hj) * p.o_sh;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = kHalfD * half; c < kHalfD * (half + 1); c += 32) {
         uint32_t v[32];
         tmem_ld32(tO + lane_off + c, v);
         tmem_wait_ld();
