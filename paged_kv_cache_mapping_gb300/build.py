@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_api.cu", "pkv_append.cu", "pkv_decode.cu", "pkv_prefill.cu", "pkv_f32.cu", "pkv_static_ws.cu", "pkv_prefill_tc.cu", "pkv_blocks.cu"]
+SOURCES = ["pkv_api.cu", "pkv_append.cu", "pkv_plan.cu", "pkv_decode.cu", "pkv_prefill.cu", "pkv_f32.cu", "pkv_static_ws.cu", "pkv_prefill_tc.cu", "pkv_blocks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               f"-I{os.path.join(ROOT, 'include')}", f"-I{CSRC}"]

@@ -1,0 +1,203 @@
+// pkv_plan.cu -- the device-side plan of one attention call: per-sequence
+// work counts, their prefix sums and the work lists of the decode and
+// prefill kernels, built from the device lengths with no host round trip.
+//
+// Decode rows are cut into chunks whose length depends only on the
+// sequence's visible key count (128 * 2^k tokens, at most 128 chunks), so
+// results depend neither on the batch nor on the page layout ("How Easy Is
+// It to Start Serving LLMs?", "3. Load balancing": long requests are split
+// into chunks and a merge step stitches them).  Prefill rows are cut into
+// tiles of query tokens, the last tokens (most keys) first.
+#include "pkv_pipeline.cuh"
+
+namespace pkv {
+
+// ---------------------------------------------------------------- plan
+// Block-wide exclusive scan of K counts per thread (warp shuffles, then one
+// warp over the warp totals).  off[] = the thread's offsets, totals[] = the
+// block totals.
+template <int K>
+__device__ __forceinline__ void block_scan(const int (&v)[K], int (&off)[K], int (&totals)[K]) {
+  __shared__ int wsum[32][K];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) x[k] = v[k];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
+  }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < K; ++k) wsum[warp][k] = x[k];
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      int y = lane < nw ? wsum[lane][k] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int z = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += z;
+      }
+      if (lane < nw) wsum[lane][k] = y;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    off[k] = x[k] - v[k] + (warp > 0 ? wsum[warp - 1][k] : 0);
+    totals[k] = wsum[nw - 1][k];
+  }
+}
+
+// First key a decoding query (position n - 1) sees.
+__device__ __forceinline__ int decode_first_key(const AttnParams& p, int n) {
+  return p.window_left >= 0 && n - 1 - p.window_left > 0 ? n - 1 - p.window_left : 0;
+}
+
+// Work counts of sequence s: decode chunks (all, full, ragged last) or
+// prefill tiles.  Inconsistent lengths give no work (and are recorded).
+struct SeqCounts {
+  int dec, full, tail, pf;  // decode chunks (all, full, ragged last), prefill tiles
+  int n, t0, q_s;           // the lengths they came from
+};
+
+__device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool record) {
+  const int c0 = __ldg(p.cu_q + s), c1 = __ldg(p.cu_q + s + 1);
+  const int q_s = c1 - c0;
+  const int n = __ldg(p.seq_lens + s);
+  SeqCounts c{0, 0, 0, 0, n, c0, q_s};
+  if (q_s == 0) return c;
+  if (q_s < 0 || q_s > n || (int64_t)n > (int64_t)p.max_blocks * p.bs || c0 < 0 || c1 > p.T) {
+    if (record) atomicOr(p.err, kErrLengths);
+    return c;
+  }
+  if (q_s == 1 && p.G <= p.decode_max_g) {
+    // the visible keys [lo, n) are cut into chunks of 2^k from lo
+    const int lo = decode_first_key(p, n);
+    const int k = chunk_shift(n - lo);
+    c.dec = (int)(((unsigned)(n - lo) + (1u << k) - 1u) >> k);
+    c.full = (n - lo) >> k;
+    c.tail = c.dec - c.full;
+  } else {
+    c.pf = p.pf_tq > 0 ? (q_s + p.pf_tq - 1) / p.pf_tq
+                       : (int)(((int64_t)q_s * p.G + kPrefillRows - 1) / kPrefillRows);
+  }
+  return c;
+}
+
+// Descriptor of decode chunk ch of sequence s: off0 is the sequence's first
+// entry in the per-sequence chunk numbering, off1 / off2 its first full /
+// ragged chunk in the work list, where all full chunks (tot_full of them)
+// come before the ragged ones.
+__device__ __forceinline__ void write_dec_desc(const AttnParams& p, int s, const SeqCounts& c, int off0, int off1,
+                                               int off2, int tot_full, int ch) {
+  const int first = decode_first_key(p, c.n);
+  const int k = chunk_shift(c.n - first);
+  const int k0 = first + (ch << k);
+  int4* dst = reinterpret_cast<int4*>(p.ws.dec_desc + (ch < c.full ? off1 + ch : tot_full + off2));
+  dst[0] = make_int4(s, k0, min(k0 + (1 << k), c.n), c.t0);
+  dst[1] = make_int4(c.dec, off0, ch, 0);
+}
+
+// Descriptor of prefill tile qt of sequence s (its tiles start at off3).
+__device__ __forceinline__ void write_pf_desc(const AttnParams& p, int s, const SeqCounts& c, int off3, int qt) {
+  int4* dst = reinterpret_cast<int4*>(p.ws.pf_desc + off3 + qt);
+  dst[0] = make_int4(s, c.t0, c.q_s, c.n);
+  if (p.pf_tq > 0) {  // query tokens r0 .. r1-1, the last tokens (most keys) first
+    const int r1 = c.q_s - qt * p.pf_tq, r0 = max(0, r1 - p.pf_tq);
+    dst[1] = make_int4(r0, r1, c.n - c.q_s + r1, 0);
+  } else {  // (token, head) rows r0 .. r1-1
+    const int r0 = qt * kPrefillRows, r1 = min(r0 + kPrefillRows, c.q_s * p.G);
+    dst[1] = make_int4(r0, r1, c.n - c.q_s + (r1 - 1) / p.G + 1, 0);
+  }
+}
+
+// Batches up to this size write their lists one warp per sequence (one lane
+// per chunk or tile); larger ones one thread per sequence.
+constexpr int kPlanSeqs = 512;
+
+// One block: per-sequence work counts and their prefix sums, the decode
+// work list (every full chunk first, then the ragged last chunks, so that
+// the small pieces come last), the list of split sequences, the prefill
+// tile list, and the per-call counters reset.  Reads device lengths; no
+// host round trip.
+__global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
+  launch_dependents();  // the decode kernel may start its set-up now
+  const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
+  const int B = p.B;
+  const int per = (B + nth - 1) / nth;
+  const int s0 = min(tid * per, B), s1 = min(s0 + per, B);
+  // First pass, counts and their prefix sums.  It reads only the lengths,
+  // which no kernel of this library writes, so it runs before the wait
+  // below, while the previous kernel (e.g. the append) is still running.
+  SeqCounts first{};  // the thread's first sequence, kept for the second pass
+  int sum[5] = {0, 0, 0, 0, 0};
+  for (int s = s0; s < s1; ++s) {
+    const SeqCounts c = seq_counts(p, s, true);
+    if (s == s0) first = c;
+    sum[0] += c.dec;
+    sum[1] += c.full;
+    sum[2] += c.tail;
+    sum[3] += c.pf;
+    sum[4] += c.dec > 1;
+  }
+  int off[5], tot[5];
+  block_scan<5>(sum, off, tot);
+  // launched with programmatic dependent launch: the workspace may still be
+  // read by the previous attention call's kernels until the previous kernel
+  // has completed
+  grid_dep_wait();
+  __shared__ int4 sq_cnt[kPlanSeqs];  // dec, full, pf, n
+  __shared__ int4 sq_off[kPlanSeqs];  // off[0..3]
+  __shared__ int2 sq_len[kPlanSeqs];  // t0, q_s
+  const bool by_warp = B <= kPlanSeqs;
+  for (int s = s0; s < s1; ++s) {
+    const SeqCounts c = s == s0 ? first : seq_counts(p, s, false);
+    p.ws.dec_off[s] = off[0];
+    p.ws.pf_off[s] = off[3];
+    if (c.dec > 1) p.ws.merge_list[off[4]] = s;
+    if (by_warp) {
+      sq_cnt[s] = make_int4(c.dec, c.full, c.pf, c.n);
+      sq_off[s] = make_int4(off[0], off[1], off[2], off[3]);
+      sq_len[s] = make_int2(c.t0, c.q_s);
+    } else {
+      for (int ch = 0; ch < c.dec; ++ch) write_dec_desc(p, s, c, off[0], off[1], off[2], tot[1], ch);
+      for (int qt = 0; qt < c.pf; ++qt) write_pf_desc(p, s, c, off[3], qt);
+    }
+    off[0] += c.dec;
+    off[1] += c.full;
+    off[2] += c.tail;
+    off[3] += c.pf;
+    off[4] += c.dec > 1;
+  }
+  if (by_warp) {
+    __syncthreads();
+    for (int s = warp; s < B; s += nw) {
+      const int4 cn = sq_cnt[s], of = sq_off[s];
+      const int2 ln = sq_len[s];
+      const SeqCounts c{cn.x, cn.y, cn.x - cn.y, cn.z, cn.w, ln.x, ln.y};
+      for (int ch = lane; ch < c.dec; ch += 32) write_dec_desc(p, s, c, of.x, of.y, of.z, tot[1], ch);
+      for (int qt = lane; qt < c.pf; qt += 32) write_pf_desc(p, s, c, of.w, qt);
+    }
+  }
+  if (tid == 0) {
+    p.ws.dec_off[B] = tot[0];
+    p.ws.pf_off[B] = tot[3];
+    *p.ws.work = 0;
+    *p.ws.pf_work = 0;
+    *p.ws.n_merge = tot[4];
+  }
+  for (int i = tid; i < B * p.Hkv; i += nth) p.ws.done[i] = 0;
+}
+
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t st) {
+  return launch_ex(plan_kernel, dim3(1), dim3(1024), 0, st, true, p);
+}
+
+}  // namespace pkv
