@@ -108,94 +108,71 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   return v;
 }
 
-// A warp merges the chunk results of query heads hq0 + j * stride,
-// j < nh (nh <= 4), of a split sequence: lane c holds the weights of chunks
-// c, c+32, ..; lane l accumulates output elements 4l .. 4l+3.  The loads of
-// four chunks are issued together before they are used.
+// A warp merges the chunk results of query head hq of a split sequence:
+// lane c holds the weights of chunks c, c+32, ..; lane l accumulates output
+// elements 4l .. 4l+3.  The loads of sixteen chunks are issued together
+// before they are used.
 // o = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M), chunks in order.
 template <typename OutT, int D>
-__device__ __noinline__ void merge_heads(const AttnParams& p, int u0, int n, int hq0, int stride, int nh, int t,
-                                         int lane) {
+__device__ __noinline__ void merge_head1(const AttnParams& p, int u0, int n, int hq, int t, int lane) {
   constexpr int kQ = kMaxChunks / 32;  // chunks per lane
-  constexpr int kB = 4;                // chunks per batch of loads
-  float wv[4][kQ];
-  float inv_l[4];
+  constexpr int kB = 16;               // chunks per batch of loads
+  float wv[kQ], lv[kQ];
+  float M = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int k = 0; k < kQ; ++k) wv[j][k] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j >= nh) break;
-    const int h = hq0 + j * stride;
-    float lv[kQ];
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kQ; ++k) {
-      const int c = lane + 32 * k;
-      lv[k] = c < n ? __ldcg(p.ws.part_lse + (int64_t)(u0 + c) * p.Hq + h) : -INFINITY;
-      M = fmaxf(M, lv[k]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-#pragma unroll
-    for (int k = 0; k < kQ; ++k) {
-      wv[j][k] = lane + 32 * k < n ? exp2f(lv[k] - M) : 0.f;
-      L += wv[j][k];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    inv_l[j] = 1.f / L;
+  for (int k = 0; k < kQ; ++k) {
+    const int c = lane + 32 * k;
+    lv[k] = c < n ? __ldcg(p.ws.part_lse + (int64_t)(u0 + c) * p.Hq + hq) : -INFINITY;
+    M = fmaxf(M, lv[k]);
   }
-  const bool act = lane * 4 < D;
-  float4 acc[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* base = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)u0 * p.Hq * D) + lane;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f;
+#pragma unroll
+  for (int k = 0; k < kQ; ++k) {
+    wv[k] = lane + 32 * k < n ? exp2f(lv[k] - M) : 0.f;
+    L += wv[k];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv_l = 1.f / L;
+  const bool act = lane * 4 < D;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* base = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)u0 * p.Hq * D) +
+                       (int64_t)hq * (D / 4) + lane;
   const int64_t cstep = (int64_t)p.Hq * D / 4;  // float4s between chunks
 #pragma unroll
   for (int k = 0; k < kQ; ++k) {
     if (32 * k >= n) break;
+#pragma unroll
     for (int cb = 0; cb < 32; cb += kB) {
       if (32 * k + cb >= n) break;
-      float4 v[kB][4];
+      float4 v[kB];
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
         const int c = 32 * k + cb + b;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          v[b][j] = (act && c < n && j < nh)
-                        ? __ldcg(base + c * cstep + (int64_t)(hq0 + j * stride) * (D / 4))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[b] = act && c < n ? __ldcg(base + c * cstep) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float wc = __shfl_sync(0xffffffffu, wv[j][k], cb + b);  // 0 past n
-          acc[j].x += wc * v[b][j].x;
-          acc[j].y += wc * v[b][j].y;
-          acc[j].z += wc * v[b][j].z;
-          acc[j].w += wc * v[b][j].w;
-        }
+        const float wc = __shfl_sync(0xffffffffu, wv[k], cb + b);  // 0 past n
+        acc.x += wc * v[b].x;
+        acc.y += wc * v[b].y;
+        acc.z += wc * v[b].z;
+        acc.w += wc * v[b].w;
       }
     }
   }
   if (!act) return;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j >= nh) break;
-    OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + j * stride) * p.o_sh + 4 * lane;
-    store2(dst, acc[j].x * inv_l[j], acc[j].y * inv_l[j]);
-    store2(dst + 2, acc[j].z * inv_l[j], acc[j].w * inv_l[j]);
-  }
+  OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)hq * p.o_sh + 4 * lane;
+  store2(dst, acc.x * inv_l, acc.y * inv_l);
+  store2(dst + 2, acc.z * inv_l, acc.w * inv_l);
 }
 
 // Item descriptor as published in the item ring.
 enum : int { kItemDecode = 0, kItemMerge = 1 };
 struct ItemMeta {
-  int s, k0, k1, t, nchunks, u, hg, u0, kind;
+  int s, k0, k1, t, nchunks, u, hg, u0, kind;  // u: the chunk of a decode item, the part of a merge item
 };
 
 template <int KV, int D, typename OutT>
@@ -239,8 +216,11 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
   grid_dep_wait();  // the plan kernel's lists are complete from here on
   if (warp > HP + 1) return;  // launched with (HP + 2) warps; nothing else to do
   const int HG = p.Hkv / HP;
-  const int n_dec = p.ws.dec_off[p.B] * HG;     // decode items, then
-  const int n_items = n_dec + *p.ws.n_merge * HG;  // merge items
+  // a merge is cut into G parts of HP query heads (one per consumer warp),
+  // so that the merges of the last sequences spread over many CTAs
+  const int MS = p.G;
+  const int n_dec = p.ws.dec_off[p.B] * HG;          // decode items, then
+  const int n_items = n_dec + *p.ws.n_merge * HG * MS;  // merge items
 
   if (warp == HP) {
     // ======================= copy warp =======================
@@ -390,10 +370,11 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
             bulk_g2s(smem_u32(it + r * QRowB), q0 + (int64_t)r * p.q_sh, QRowB, ifull0 + 8 * islot);
         }
       } else {
-        const int hg = (x - n_dec) % HG;
-        const int sm = p.ws.merge_list[(x - n_dec) / HG];
+        const int part = (x - n_dec) % MS, rest = (x - n_dec) / MS;
+        const int hg = rest % HG;
+        const int sm = p.ws.merge_list[rest / HG];
         const int u0 = p.ws.dec_off[sm];
-        const ItemMeta mm{sm, 0, 0, p.cu_q[sm], p.ws.dec_off[sm + 1] - u0, 0, hg, u0, kItemMerge};
+        const ItemMeta mm{sm, 0, 0, p.cu_q[sm], p.ws.dec_off[sm + 1] - u0, part, hg, u0, kItemMerge};
         if (lane == 0) {
           *mp = mm;
           mbar_arrive(ifull0 + 8 * islot);
@@ -512,11 +493,9 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
       ready = __shfl_sync(0xffffffffu, ready, 0);
       __syncwarp();
       if (ready) {
-        // the HP warps split the group's HP * G query heads: warp h takes
-        // heads h, h + HP, .. (at most 4 each; more are done in rounds)
-        const int nq = HP * G, q0 = m.hg * nq;
-        for (int r = h; r < nq; r += 4 * HP)
-          merge_heads<OutT, D>(p, m.u0, m.nchunks, q0 + r, HP, min(4, (nq - r + HP - 1) / HP), m.t, lane);
+        // part m.u of the group's HP * G query heads: HP heads, warp h
+        // merges one of them
+        merge_head1<OutT, D>(p, m.u0, m.nchunks, m.hg * HP * G + m.u * HP + h, m.t, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(iempty0 + 8 * islot);
