@@ -541,6 +541,50 @@ def run_reference(args, rank, world, budget_s=90.0):
 
 
 # ------------------------------------------------------------------ main
+def run_layout_compare(args):
+    """Scattered against contiguous block tables on the layout workloads
+    (B 32 x 2048 keys, block sizes 1, 16, 64): each repeat allocates fresh
+    caches for each layout (alternating which goes first) and times 200
+    back-to-back pkv_attention calls over 4 rotated layer caches with CUDA
+    events.  Reports per-layout medians and their ratio."""
+    import torch
+    from paged_kv_cache_mapping_gb300 import harness, pkv_device_errors
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    calls, layers = 200, 4
+    times = {}
+    for r in range(args.repeats):
+        for bs in (1, 16, 64):
+            for contiguous in ((False, True) if r % 2 == 0 else (True, False)):
+                wl = W.layout_sweep(bs, contiguous, seed=1003)
+                ds = harness.DeviceStep(wl, out_dtype=torch.bfloat16, layers=layers, max_q_len=1)
+                for i in range(max(args.warmup, 3) * layers):
+                    ds.attention_only(i % layers)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for i in range(calls):
+                    ds.attention_only(i % layers)
+                b.record()
+                torch.cuda.synchronize()
+                if pkv_device_errors(dev):
+                    raise RuntimeError("device error flags set in the layout comparison")
+                times.setdefault((bs, contiguous), []).append(a.elapsed_time(b) / calls * 1e3)
+                del ds
+                torch.cuda.empty_cache()
+    rows = []
+    for bs in (1, 16, 64):
+        s, c = statistics.median(times[(bs, False)]), statistics.median(times[(bs, True)])
+        rows.append({"block_size": bs, "scattered_us": round(s, 2), "contiguous_us": round(c, 2),
+                     "ratio": round(s / c, 4)})
+    return {"metric": "pkv_attention time, scattered / contiguous block tables", "unit": "ratio",
+            "value": max(r["ratio"] for r in rows), "higher_is_better": False, "repeats": args.repeats,
+            "config": {"workload": "layout B32 ctx2048, Qwen3-4B heads, bf16, block sizes 1/16/64",
+                       "timing": f"median over repeats of {calls} back-to-back calls, {layers} layer caches rotated"},
+            "rows": rows}
+
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,6 +597,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soft-cap", type=float, default=0.0, help="logits soft cap (variant; 0: off)")
     ap.add_argument("--window-left", type=int, default=-1, help="sliding window (variant; < 0: off)")
+    ap.add_argument("--layout-compare", action="store_true",
+                    help="print scattered / contiguous attention time on the layout workloads instead")
+    ap.add_argument("--repeats", type=int, default=8, help="fresh allocations per layout (--layout-compare)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -560,7 +607,9 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     if world != args.gpus:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N > 1 with torch.distributed.run")
-    if args.impl == "reference":
+    if args.layout_compare:
+        line = run_layout_compare(args) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         if world > 1:
