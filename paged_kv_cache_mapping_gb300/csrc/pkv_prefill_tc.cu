@@ -156,15 +156,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// p0, p1 >= 0 -> bf16 pairs hi + lo by truncation: hi keeps the upper 16
-// bits of each fp32 value, lo the upper 16 bits of the exact remainder
-// p - hi; hi + lo carries about 16 significant bits (relative error below
-// 2^-16) with integer and bit operations only.  Element 0 in the low halves.
-__device__ __forceinline__ void split_trunc_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-  hi = __byte_perm(u0, u1, 0x7632);
-  const float r0 = p0 - __uint_as_float(u0 & 0xFFFF0000u), r1 = p1 - __uint_as_float(u1 & 0xFFFF0000u);
-  lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+// Packed pairs of fp32 (sm_100 f32x2 arithmetic): one instruction does two
+// lanes' worth of the FMA-pipe work, which leaves more issue slots to the
+// MMA-issuing warp that shares a scheduler with softmax warps.
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void up2(unsigned long long v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // Work unit u: prefill tile u / Hkv (tokens r0 .. r1-1 of its sequence,
@@ -565,18 +581,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // of tile gg - 2 that read this buffer finished before its Q K^T ran.
         const float ms = m == -INFINITY ? 0.f : m;
         {
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums, kept apart for latency
+          // keys 2w, 2w + 1 as one packed pair: exponent argument, row sum
+          // and the lo residual each take one f32x2 instruction per pair.
+          // hi keeps the upper 16 bits of each p (bf16 by truncation), lo the
+          // upper 16 bits of the exact remainder p - hi: hi + lo carries about
+          // 16 significant bits.  Key 2w in the low halves.
+          const unsigned long long xs2 = pk2(xs, xs), nms2 = pk2(-ms, -ms);
+          unsigned long long s2[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};  // partial sums, kept apart for latency
           uint32_t hi[32], lo[32];
 #pragma unroll
           for (int w = 0; w < 32; ++w) {
-            const float p0 = ex2_approx(fmaf(x[2 * w], xs, -ms));
-            const float p1 = ex2_approx(fmaf(x[2 * w + 1], xs, -ms));
-            s4[w & 3] += p0 + p1;
-            split_trunc_bf16(p0, p1, hi[w], lo[w]);
+            float a0, a1;
+            up2(fma2(pk2(x[2 * w], x[2 * w + 1]), xs2, nms2), a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            const unsigned long long pp = pk2(p0, p1);
+            s2[w & 1] = add2(s2[w & 1], pp);
+            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+            hi[w] = __byte_perm(u0, u1, 0x7632);
+            float r0, r1;  // p - hi exactly: the truncated-away low bits
+            up2(sub2(pp, pk2(__uint_as_float(u0 & 0xFFFF0000u), __uint_as_float(u1 & 0xFFFF0000u))), r0, r1);
+            lo[w] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
           }
           tmem_st32(ts + 32 * half, hi);
           tmem_st32(ts + kHalfKeys + 32 * half, lo);
-          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          float t0, t1, t2, t3;
+          up2(s2[0], t0, t1);
+          up2(s2[1], t2, t3);
+          l += (t0 + t1) + (t2 + t3);
         }
         tmem_wait_st();
         tc_fence_before();
