@@ -46,7 +46,7 @@
  * split-KV chunks and the log-sum-exp merge that the pages describe reach
  * this same value (up to rounding order); the oracle does none of them.
  *
- * Readings of points the pages leave open (each listed in the design doc):
+ * Readings of points the pages leave open:
  *   - slot = block_table[p / block_size] * block_size + p % block_size.
  *   - seq_lens counts this step's appended tokens; query i of a sequence with
  *     q_s new tokens and N keys sits at position p = N - q_s + i and sees
