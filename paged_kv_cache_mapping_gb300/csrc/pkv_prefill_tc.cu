@@ -159,6 +159,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // Packed pairs of fp32 (sm_100 f32x2 arithmetic): one instruction does two
 // lanes' worth of the FMA-pipe work, which leaves more issue slots to the
 // MMA-issuing warp that shares a scheduler with softmax warps.
+// three-input max (sm_100): exact, like two fmaxf
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ unsigned long long pk2(float a, float b) {
   unsigned long long r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -543,9 +550,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float t8[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) t8[j] = x[j];
+          static_assert(kHalfKeys == 64, "the reduction below covers 64 keys");
 #pragma unroll
-          for (int c = 8; c < kHalfKeys; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
-          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+          for (int c = 8; c < 56; c += 16)  // keys 8 .. 55, two per step
+#pragma unroll
+            for (int j = 0; j < 8; ++j) t8[j] = fmax3(t8[j], x[c + j], x[c + 8 + j]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t8[j] = fmaxf(t8[j], x[56 + j]);  // keys 56 .. 63
+          mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
           float other;
           if (!trade(mx, other)) { ok = false; break; }
           mx = fmaxf(mx, other) * xs;
