@@ -9,10 +9,13 @@
 // 128 keys is a dense contraction, run here as
 //     S = Q K^T      (M 128, N 128 keys, K = D; bf16 in, fp32 in TMEM)
 //     O += P V       (M 128, N = D, K 128 keys; P split into bf16 hi + lo)
-// with an online softmax (base 2) between them, one thread per query row.
-// P never leaves tensor memory: each softmax thread overwrites its row of S
+// with an online softmax (base 2) between them, two threads per query row.
+// P never leaves tensor memory: the softmax threads overwrite their row of S
 // with the hi and lo bf16 parts of P (64 packed columns each) and the P V
-// MMAs read their A operand from there.  An M 128 x N 128 x K 16 MMA keeps
+// MMAs read their A operand from there.  The softmax arithmetic runs as
+// packed f32x2 operations where it can: the MMA-issuing warp shares a
+// scheduler with two softmax warps, and a dense stream of FMA-pipe
+// instructions there delays its MMA issues.  An M 128 x N 128 x K 16 MMA keeps
 // the tensor core at its full rate; N 64 would run at about two thirds.
 //
 // CTA (one per SM, persistent over tiles), 11 warps:
