@@ -566,7 +566,9 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
     const int64_t dec_seqs = std::min<int64_t>(B, T);
     // right after the plan the decode kernel may overlap its start with the
     // plan's end (it waits for the plan's lists on the device)
-    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * pkv::max_chunks_for(max_ctx) * Hkv, sms, st, !prefill);
+    // programmatic launch after the plan, and after the tensor-core prefill
+    // (which waits for the plan itself); the mma.sync prefill is a plain launch
+    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * pkv::max_chunks_for(max_ctx) * Hkv, sms, st, !prefill || tc);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return finish(st, "pkv_attention");

@@ -202,6 +202,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using Geo = TcGeom<D>;
+  // launched with programmatic dependent launch right after the plan: wait
+  // for its lists (every thread, before any global access), then let the
+  // decode kernel that follows launch and set up on the SMs this grid frees
+  grid_dep_wait();
+  launch_dependents();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sQ = smem_u32(smem + Geo::kOffQ);
@@ -716,8 +721,7 @@ cudaError_t launch_tc(const AttnParams& p, int64_t max_units, int num_sms, cudaS
   int64_t grid = num_sms;
   if (grid > max_units) grid = max_units;
   if (grid < 1) return cudaSuccess;
-  kern<<<(unsigned)grid, kTcThreads, Geo::kSmem, st>>>(p, mq, mk, mv);
-  return cudaGetLastError();
+  return launch_ex(kern, dim3((unsigned)grid), dim3(kTcThreads), Geo::kSmem, st, true, p, mq, mk, mv);
 }
 
 }  // namespace
