@@ -651,9 +651,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld32(tO + lane_off + c, v);
         tmem_wait_ld();
         if (valid) {
+          OutT* d = dst + c;
+          if ((reinterpret_cast<uintptr_t>(d) & 15u) == 0) {  // 16-byte stores (same rounding as store2)
+            constexpr int kPer = 16 / (int)sizeof(OutT);     // elements per store
 #pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            store2(dst + c + j, __uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+            for (int j = 0; j < 32; j += kPer) {
+              uint4 w;
+              uint32_t* wu = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if constexpr (sizeof(OutT) == 2) {
+                  wu[e] = pack_bf16(__uint_as_float(v[j + 2 * e]) * inv, __uint_as_float(v[j + 2 * e + 1]) * inv);
+                } else {
+                  wu[e] = __float_as_uint(__uint_as_float(v[j + e]) * inv);
+                }
+              }
+              *reinterpret_cast<uint4*>(d + j) = w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              store2(d + j, __uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+          }
         }
       }
       tc_fence_before();
