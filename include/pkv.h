@@ -50,6 +50,15 @@
  * is skipped (no write, zero contribution) and recorded; check mode, or
  * pkv_device_errors(), reports it.  No kernel traps or faults on bad
  * indices.
+ *
+ * Kernels of this library are launched with programmatic dependent launch:
+ * each may begin (and set up) while the previous kernel in the stream is
+ * still running, and waits for it before touching memory, with one
+ * exception: the plan kernel of pkv_attention reads cu_seqlens_q and
+ * seq_lens before that wait.  This is safe whenever those arrays are final
+ * when the previous kernel in the stream lets its successor start early --
+ * always, when that kernel is one of this library's (none of them writes
+ * the lengths) or a kernel that does not use programmatic launch itself.
  */
 #ifndef PKV_H_
 #define PKV_H_
