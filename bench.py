@@ -37,6 +37,7 @@ WORKLOADS = ("decode", "layout-bs1-scattered", "layout-bs1-contiguous", "layout-
              "layout-bs16-contiguous", "layout-bs64-scattered", "layout-bs64-contiguous", "mixed",
              "long-fp8", "lognormal-fp8")
 DECODE_SOURCES = ["pkv_decode.cu", "pkv_pipeline.cuh", "pkv_common.cuh"]
+PREFILL_SOURCES = ["pkv_prefill_tc.cu", "pkv_common.cuh"]
 
 
 # ------------------------------------------------------------------ accounting
@@ -79,14 +80,14 @@ def traffic_record():
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("source_sha256") != decode_source_hash():
+    if rec.get("source_sha256") != source_hash(DECODE_SOURCES):
         return None
     return rec
 
 
-def decode_source_hash():
+def source_hash(names):
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_mapping_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -95,9 +96,11 @@ def decode_source_hash():
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """SM clocks, power and clock-event (throttle) reasons sampled while the
-    timed region runs: NVML read through ctypes every 10 ms from a thread
-    (nothing is set, only read), else nvidia-smi every 100 ms.  Samples taken
-    before __enter__ returns are not counted."""
+    timed regions run: NVML read through ctypes every millisecond from a
+    thread (nothing is set, only read), else nvidia-smi every 100 ms.  Only
+    samples taken while the sampler is armed count; arm() takes one sample at
+    once and disarm() one more, so that a timed region of a few milliseconds
+    still carries samples."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -106,12 +109,15 @@ class ClockSampler:
     BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
             "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval=0.001):
         self.gpu = gpu_index
+        self.interval = interval
         self.rows = []  # (sm_mhz, max_mhz, power_w, reasons_mask)
         self.source = None
         self.proc = None
         self.thread = None
+        self.armed = False
+        self.regions = 0
 
     def _nvml(self):
         import ctypes
@@ -127,27 +133,35 @@ class ClockSampler:
             raise OSError("nvmlDeviceGetHandleByIndex failed")
         return lib, h
 
-    def _poll(self, lib, h):
+    def _sample(self):
         import ctypes
-        sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
-        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        lib, h = self.lib, self.h
+        sm, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0  # NVML_CLOCK_SM
+        lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+        if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) != 0:
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(rs))
+        if ok:
+            self.rows.append((float(sm.value), float(self.max_mhz), mw.value / 1000.0, int(rs.value)))
+
+    def _poll(self):
         while not self.stop:
-            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0
-            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
-            if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) != 0:
-                lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(rs))
-            if ok and self.armed:
-                self.rows.append((float(sm.value), float(mx.value), mw.value / 1000.0, int(rs.value)))
-            time.sleep(0.01)
+            if self.armed:
+                self._sample()
+            time.sleep(self.interval)
 
     def __enter__(self):
+        import ctypes
         import threading
-        self.stop, self.armed = False, False
+        self.stop = False
         try:
-            lib, h = self._nvml()
-            self.thread = threading.Thread(target=self._poll, args=(lib, h), daemon=True)
+            self.lib, self.h = self._nvml()
+            mx = ctypes.c_uint()
+            self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.thread = threading.Thread(target=self._poll, daemon=True)
             self.thread.start()
-            self.source = "nvml 10 ms"
+            self.source = f"nvml {self.interval * 1e3:g} ms"
         except (OSError, AttributeError, IndexError, ValueError):
             self.thread = None
             try:
@@ -156,15 +170,21 @@ class ClockSampler:
                 self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                               "--format=csv,noheader,nounits", "-lms", "100"],
                                              stdout=self.f, stderr=subprocess.DEVNULL)
-                self.source = "nvidia-smi 100 ms"
-                t0 = time.time()
-                while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
-                    time.sleep(0.05)
-                self.skip = open(self.path).read().count("\n")
+                self.source = "nvidia-smi 100 ms (whole run)"
             except (OSError, FileNotFoundError):
                 self.proc = None
-        self.armed = True
         return self
+
+    def arm(self):
+        self.regions += 1
+        if self.thread is not None:
+            self._sample()
+        self.armed = True
+
+    def disarm(self):
+        if self.thread is not None and self.armed:
+            self._sample()
+        self.armed = False
 
     def __exit__(self, *a):
         self.armed = False
@@ -180,7 +200,7 @@ class ClockSampler:
             self.f.close()
             names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
             with open(self.path) as f:
-                lines = f.read().splitlines()[self.skip:]
+                lines = f.read().splitlines()
             os.remove(self.path)
 
             def num(x):
@@ -202,7 +222,8 @@ class ClockSampler:
         reasons = sorted(n for n, b in self.BITS.items() if any(r[3] & b for r in self.rows))
         return {"sm_mhz": statistics.median(r[0] for r in self.rows),
                 "sm_max_mhz": max(r[1] for r in self.rows), "reasons": reasons, "samples": len(self.rows),
-                "power_w_max": round(max(r[2] for r in self.rows), 1), "source": self.source}
+                "timed_regions": self.regions, "power_w_max": round(max(r[2] for r in self.rows), 1),
+                "source": self.source}
 
 
 # ------------------------------------------------------------------ ranks
@@ -223,11 +244,51 @@ def job_rate(ms_step, step_bytes, world, device):
 
 
 # ------------------------------------------------------------------ our arm
+# Layers of one Qwen3-4B decode step.  The pages plan a step once and reuse
+# the plan for the attention of every layer ("How Easy Is It to Start
+# Serving LLMs?", "3. Load balancing: keep every SM busy"); the slot mapping
+# is likewise made once per step.  A benchmark step is one layer.
+LAYERS_PER_MODEL_STEP = 36
+
+
+def layer_loop(ds, steps, layers, on_run=None):
+    """steps consecutive layer steps from the start of a model step: slot
+    mapping and plan at every model-step boundary, then append + attention
+    run of the layer (on_run(i, fn) wraps the attention run, e.g. with
+    events)."""
+    from paged_kv_cache_mapping_gb300 import pkv_append
+    wl = ds.wl
+    for i in range(steps):
+        if i % LAYERS_PER_MODEL_STEP == 0:
+            ds.model_step_start()
+        layer = i % layers
+        kc, vc = ds.caches[layer]
+        pkv_append(ds.k_new, ds.v_new, ds.slots, kc, vc, wl.k_scale, wl.v_scale)
+        if on_run is None:
+            ds.run(layer)
+        else:
+            on_run(i, lambda: ds.run(layer))
+
+
+def timed_runs(ds, steps, layers, stream):
+    """The attention run alone, with CUDA events on the launching stream
+    around each call, inside the layer loop; returns ms per call."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def on_run(i, fn):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    layer_loop(ds, steps, layers, on_run)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def run_ours(args, rank, world):
     import torch
 
-    from paged_kv_cache_mapping_gb300 import (harness, pkv_append, pkv_attention, pkv_device_errors,
-                                              pkv_slot_mapping)
+    from paged_kv_cache_mapping_gb300 import harness, pkv_device_errors
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -242,59 +303,61 @@ def run_ours(args, rank, world):
     nb = step_bytes(wl, window_left=args.window_left)
     stream = torch.cuda.current_stream(dev)
 
-    for i in range(args.warmup):
-        ds.step(i % LAYERS)
+    layer_loop(ds, args.warmup, LAYERS)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        clk.arm()
         t_start.record(stream)
-        for i in range(args.steps):
-            kc, vc = ds.caches[i % LAYERS]
-            pkv_slot_mapping(ds.cu_q, ds.seq_lens, ds.bt, wl.block_size, out=ds.slots)
-            pkv_append(ds.k_new, ds.v_new, ds.slots, kc, vc, wl.k_scale, wl.v_scale)
-            pkv_attention(ds.q, ds.cu_q, ds.seq_lens, ds.bt, kc, vc, wl.scale, ds.out, wl.k_scale,
-                          wl.v_scale, max_q, ds.ws, soft_cap=args.soft_cap, window_left=args.window_left)
+        layer_loop(ds, args.steps, LAYERS)
         t_end.record(stream)
         torch.cuda.synchronize()
-    flags = pkv_device_errors(dev)
-    if flags:
-        raise RuntimeError(f"device error flags 0x{flags:x} in the timed region")
-    total_ms = t_start.elapsed_time(t_end)
-    ms_step = total_ms / args.steps
-    # The attention call alone, for the roofline: the same steps again with
-    # events around each pkv_attention call.  An event recorded between two
-    # launches keeps the second from starting before the first ends, so these
-    # events stay out of the step loop above (whose kernels overlap their
-    # neighbours' launch and set-up).
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for i in range(args.steps):
-        kc, vc = ds.caches[i % LAYERS]
-        e1, e2 = ev[i]
-        pkv_slot_mapping(ds.cu_q, ds.seq_lens, ds.bt, wl.block_size, out=ds.slots)
-        pkv_append(ds.k_new, ds.v_new, ds.slots, kc, vc, wl.k_scale, wl.v_scale)
-        e1.record(stream)
-        pkv_attention(ds.q, ds.cu_q, ds.seq_lens, ds.bt, kc, vc, wl.scale, ds.out, wl.k_scale,
-                      wl.v_scale, max_q, ds.ws, soft_cap=args.soft_cap, window_left=args.window_left)
-        e2.record(stream)
-    torch.cuda.synchronize()
-    flags = pkv_device_errors(dev)
-    if flags:
-        raise RuntimeError(f"device error flags 0x{flags:x} in the attention timing pass")
-    attn_ms = [e1.elapsed_time(e2) for e1, e2 in ev]
+        clk.disarm()
+        flags = pkv_device_errors(dev)
+        if flags:
+            raise RuntimeError(f"device error flags 0x{flags:x} in the timed region")
+        ms_step = t_start.elapsed_time(t_end) / args.steps
+        # The attention run alone, for the roofline: the same steps again with
+        # events around each run.  An event recorded between two launches keeps
+        # the second from starting before the first ends, so these events stay
+        # out of the step loop above (whose kernels overlap their neighbours'
+        # launch and set-up).
+        clk.arm()
+        attn_ms = timed_runs(ds, args.steps, LAYERS, stream)
+        clk.disarm()
+        # The step as it was before plan reuse: slot mapping, append and the
+        # whole call (plan + run) in every step.
+        clk.arm()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            ds.step(i % LAYERS)
+        b.record(stream)
+        torch.cuda.synchronize()
+        clk.disarm()
+        ms_planned = a.elapsed_time(b) / args.steps
+        flags = pkv_device_errors(dev)
+        if flags:
+            raise RuntimeError(f"device error flags 0x{flags:x} in the attention timing passes")
 
-    if world > 1:
-        torch.distributed.barrier()
-    # slowest rank, every rank's bytes
-    ms_step, value = job_rate(ms_step, nb["total"], world, dev)
+        if world > 1:
+            torch.distributed.barrier()
+        # slowest rank, every rank's bytes
+        ms_step, value = job_rate(ms_step, nb["total"], world, dev)
+        _, value_planned = job_rate(ms_planned, nb["total"], world, dev)
 
-    e2e = run_e2e(ds, wl, nb, args, dev, world, max_q)
-    graph = run_graph(ds, nb, args, dev, world)
+        e2e = run_e2e(ds, wl, nb, args, dev, world, max_q, clk)
+        graph = run_graph(ds, nb, args, dev, world, clk)
+        secondary = None
+        if rank == 0 and world == 1 and args.workload == "decode" and not args.no_secondary:
+            del ds
+            torch.cuda.empty_cache()
+            secondary = run_secondary(args, dev, clk)
     if rank != 0:
         return None
     hbm, peak_kind = peaks()
@@ -309,79 +372,91 @@ def run_ours(args, rank, world):
         "config": {"workload": wl.name, "batch": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
                    "block_size": wl.block_size, "num_blocks": wl.num_blocks,
                    "mean_ctx": float(wl.seq_lens.mean()), "out_dtype": "bf16",
-                   "step": "slot mapping + append + attention (one layer)",
+                   "step": (f"one layer of a {LAYERS_PER_MODEL_STEP}-layer decode step: append of the layer's new "
+                            f"rows + attention run over the step's plan; the slot mapping and the plan are made "
+                            f"at the first layer of every model step (every {LAYERS_PER_MODEL_STEP} steps, "
+                            f"step 0 included)"),
                    "l2": f"inputs larger than L2: {LAYERS} layer cache(s) rotated, "
                          f"{nb['kv'] / 1e6:.0f} MB of live KV each",
                    "bytes_per_step": nb, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    **({"variant": {"soft_cap": args.soft_cap, "window_left": args.window_left}}
                       if args.soft_cap > 0 or args.window_left >= 0 else {})},
-        "roofline": {"bound": "hbm", "kernel": "pkv_attention (plan + decode kernels)",
+        "roofline": {"bound": "hbm", "kernel": "pkv_attention_run (decode kernel)",
                      "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
                      "traffic": rec["dram_bytes_per_launch"] if rec else None,
                      "algorithmic_bytes": nb["attention"], "avg_launch_us": round(attn_avg_ms * 1e3, 2),
-                     "timing": "CUDA events around each pkv_attention call, in a second pass over the same steps"},
+                     "timing": "CUDA events around each pkv_attention_run call, in a second pass over the same "
+                               "steps"},
+        "plan_every_step": {"value": round(value_planned, 1), "unit": UNIT, "ms_per_step": round(ms_planned, 5),
+                            "how": "slot mapping + append + pkv_attention (plan + run) in every step"},
         "e2e": e2e,
         "graph": graph,
-        # slot mapping, append, plan, decode (+ prefill)
-        "gpu_launches": (5 if max_q > 1 else 4) * args.steps,
+        # per layer: append, decode (+ prefill); per model step: slot mapping, plan
+        "gpu_launches": ((3 if max_q > 1 else 2) * args.steps
+                         + 2 * -(-args.steps // LAYERS_PER_MODEL_STEP)),
         "clocks": clk.summary(),
     }
+    if secondary is not None:
+        line["configs"] = secondary
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, nb, budget_s=args.cpu_budget)
     return line
 
 
-def run_graph(ds, nb, args, dev, world):
-    """The same step replayed from CUDA graphs (one per layer cache, captured
-    after an eager warm-up): the launch cost of the four kernels goes away.
-    Reported beside the eager value, not instead of it."""
+def run_graph(ds, nb, args, dev, world, clk):
+    """A whole model step (slot mapping, plan, then append + run for each of
+    its layers) captured into one CUDA graph after an eager warm-up and
+    replayed: the launch cost of the kernels goes away.  Reported per layer
+    beside the eager value, not instead of it."""
     import torch
     try:
         layers = len(ds.caches)
+        L = LAYERS_PER_MODEL_STEP
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
-            for layer in range(layers):
-                ds.step(layer)
+            layer_loop(ds, L, layers)
         torch.cuda.current_stream(dev).wait_stream(side)
-        graphs = []
-        for layer in range(layers):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                ds.step(layer)
-            graphs.append(g)
-        for i in range(args.warmup):
-            graphs[i % layers].replay()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer_loop(ds, L, layers)
+        for _ in range(max(1, args.warmup // L)):
+            g.replay()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         stream = torch.cuda.current_stream(dev)
+        reps = max(1, round(args.steps / L))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clk.arm()
         a.record(stream)
-        for i in range(args.steps):
-            graphs[i % layers].replay()
+        for _ in range(reps):
+            g.replay()
         b.record(stream)
         torch.cuda.synchronize()
+        clk.disarm()
         if world > 1:
             torch.distributed.barrier()
-        ms, rate = job_rate(a.elapsed_time(b) / args.steps, nb["total"], world, dev)
+        ms, rate = job_rate(a.elapsed_time(b) / (reps * L), nb["total"], world, dev)
         return {"value": round(rate, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
-                "how": "the whole step replayed from a CUDA graph per layer cache"}
+                "how": f"{reps} replay(s) of one CUDA graph holding a whole {L}-layer model step"}
     except Exception as e:  # reported, never fatal to the benchmark line
         return {"error": f"{type(e).__name__}: {e}"[:200]}
 
 
-def run_e2e(ds, wl, nb, args, dev, world, max_q):
+def run_e2e(ds, wl, nb, args, dev, world, max_q, clk):
     """Same metric through the public API with host buffers: every step
     copies the step's inputs from pinned host memory and reads the output
     back.  The inputs of a step sit in one pinned staging buffer (one
     host-to-device copy); copies run on their own stream, double-buffered,
     so that step i + 1's inputs move and step i - 1's output comes back while
-    step i computes."""
+    step i computes.  The steps are layers of model steps as in the main
+    loop: slot mapping and plan at the first layer of each."""
     import torch
 
-    from paged_kv_cache_mapping_gb300 import pkv_append, pkv_attention, pkv_slot_mapping
+    from paged_kv_cache_mapping_gb300 import (pkv_append, pkv_attention_plan, pkv_attention_run,
+                                              pkv_slot_mapping)
     src = {"q": ds.q, "k": ds.k_new, "v": ds.v_new, "cu": ds.cu_q, "sl": ds.seq_lens, "bt": ds.bt}
     off, size, total = {}, {}, 0
     for k, t in src.items():
@@ -415,10 +490,13 @@ def run_e2e(ds, wl, nb, args, dev, world, max_q):
         comp.wait_event(h2d_done[b])
         d = views[b]
         kc, vc = ds.caches[i % len(ds.caches)]
-        pkv_slot_mapping(d["cu"], d["sl"], d["bt"], wl.block_size, out=ds.slots)
+        if i % LAYERS_PER_MODEL_STEP == 0:
+            pkv_slot_mapping(d["cu"], d["sl"], d["bt"], wl.block_size, out=ds.slots)
+            pkv_attention_plan(d["q"], d["cu"], d["sl"], d["bt"], kc, ds.ws, max_q_len=max_q,
+                               window_left=args.window_left)
         pkv_append(d["k"], d["v"], ds.slots, kc, vc, wl.k_scale, wl.v_scale)
-        pkv_attention(d["q"], d["cu"], d["sl"], d["bt"], kc, vc, wl.scale, outs[b], wl.k_scale,
-                      wl.v_scale, max_q, ds.ws, soft_cap=args.soft_cap, window_left=args.window_left)
+        pkv_attention_run(d["q"], d["cu"], d["sl"], d["bt"], kc, vc, wl.scale, outs[b], ds.ws, wl.k_scale,
+                          wl.v_scale, max_q, soft_cap=args.soft_cap, window_left=args.window_left)
         comp_done[b].record(comp)
         used[b] = True
         with torch.cuda.stream(copy):
@@ -436,10 +514,12 @@ def run_e2e(ds, wl, nb, args, dev, world, max_q):
     run(args.warmup)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk.arm()
     a.record(comp)
     run(args.steps)
     b.record(comp)
     torch.cuda.synchronize()
+    clk.disarm()
     ms = a.elapsed_time(b) / args.steps
     if not torch.equal(out_h[(args.steps - 1) % 2].to(dev), outs[(args.steps - 1) % 2]):
         raise RuntimeError("end-to-end read-back differs from the device output")
@@ -452,11 +532,153 @@ def run_e2e(ds, wl, nb, args, dev, world, max_q):
                    "on a copy stream, double-buffered against the compute"}
 
 
+# ------------------------------------------------------------------ the other workloads
+def prefill_flops(wl):
+    """Algorithmic FLOPs of the prefill rows: 4 * Hq * D per visible (query
+    token, key) pair of every sequence with more than one query row."""
+    pairs = 0
+    for n, q in zip(wl.seq_lens.astype(np.int64), wl.q_lens.astype(np.int64)):
+        if q > 1:
+            pairs += int(q * (n - q) + q * (q + 1) // 2)
+    return 4 * wl.Hq * wl.D * pairs
+
+
+def time_runs(wl, dev, calls, layers=4, clk=None):
+    """ms per pkv_attention_run, back to back over rotated layer caches after
+    one plan (CUDA events at the two ends)."""
+    import torch
+
+    from paged_kv_cache_mapping_gb300 import harness, pkv_device_errors
+    ds = harness.DeviceStep(wl, device=dev, out_dtype=torch.bfloat16, layers=layers)
+    ds.model_step_start()
+    for layer in range(layers):
+        ds.layer_step(layer)
+    for i in range(3 * layers):
+        ds.run(i % layers)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.arm()
+    a.record()
+    for i in range(calls):
+        ds.run(i % layers)
+    b.record()
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.disarm()
+    if pkv_device_errors(dev):
+        raise RuntimeError(f"device error flags set on {wl.name}")
+    del ds
+    torch.cuda.empty_cache()
+    return a.elapsed_time(b) / calls
+
+
+def run_secondary(args, dev, clk):
+    """The other workloads of the survey, each as a secondary key of the
+    bench line: the page-layout ratio, the mixed chunked-prefill step with
+    the prefill's own tensor roofline, and the two fp8 workloads."""
+    hbm, peak_kind = peaks()
+    tflops, tflops_sus = tensor_peaks()
+    out = {}
+    t0 = time.time()
+    try:
+        out["layout"] = layout_ratio(dev, repeats=args.layout_repeats, clk=clk)
+    except Exception as e:  # reported, never fatal to the benchmark line
+        out["layout"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    calls = max(50, args.steps)
+    try:
+        wl = make_workload("mixed")
+        nb = step_bytes(wl)
+        ms = time_runs(wl, dev, calls, clk=clk)
+        chunks = wl.select([s for s in range(wl.B) if wl.q_lens[s] > 1])
+        fl = prefill_flops(wl)
+        ms_pf = time_runs(chunks, dev, calls, clk=clk)
+        rec = prefill_record()
+        out["mixed_prefill"] = {
+            "workload": wl.name, "call_us": round(ms * 1e3, 2),
+            "kv_gbs": round(nb["attention"] / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(nb["attention"] / (ms * 1e-3) / 1e9 / hbm, 4),
+            "prefill": {"bound": "tensor", "flops": fl, "call_us": round(ms_pf * 1e3, 2),
+                        "achieved": round(fl / (ms_pf * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                        "peak": tflops, "frac": round(fl / (ms_pf * 1e-3) / 1e12 / tflops, 4),
+                        "frac_of_sustained": round(fl / (ms_pf * 1e-3) / 1e12 / tflops_sus, 4),
+                        "tensor_pipe_active": rec.get("sm__pipe_tensor_cycles_active_pct") if rec else None,
+                        "how": "the two prefill chunks alone (the tcgen05 prefill kernel and an empty decode "
+                               "launch), back-to-back runs; FLOPs = 4 Hq D per visible (query, key) pair"}}
+    except Exception as e:
+        out["mixed_prefill"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    for name in ("long-fp8", "lognormal-fp8"):
+        try:
+            wl = make_workload(name)
+            nb = step_bytes(wl)
+            ms = time_runs(wl, dev, calls, clk=clk)
+            gbs = nb["attention"] / (ms * 1e-3) / 1e9
+            out[name.replace("-", "_")] = {"workload": wl.name, "call_us": round(ms * 1e3, 2),
+                                           "kv_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                           "algorithmic_bytes": nb["attention"]}
+        except Exception as e:
+            out[name.replace("-", "_")] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tflops, "bf16_tflops_sustained": tflops_sus,
+                    "kind": peak_kind}
+    out["how"] = (f"{calls} back-to-back pkv_attention_run calls over 4 rotated layer caches after one plan, "
+                  f"CUDA events at both ends; {time.time() - t0:.0f} s with set-up")
+    return out
+
+
+def layout_ratio(dev, repeats=2, calls=200, layers=4, clk=None):
+    """Scattered against contiguous block tables on the layout workloads (B
+    32 x 2048 keys, block sizes 1, 16, 64): each repeat allocates fresh
+    caches for each layout (alternating which goes first) and times calls
+    back-to-back runs over rotated layer caches.  Per-layout medians and
+    their ratio."""
+    times = {}
+    wls = {}
+    for r in range(repeats):
+        for bs in (1, 16, 64):
+            for contiguous in ((False, True) if r % 2 == 0 else (True, False)):
+                key = (bs, contiguous)
+                if key not in wls:
+                    wls[key] = W.layout_sweep(bs, contiguous, seed=1003)
+                times.setdefault(key, []).append(time_runs(wls[key], dev, calls, layers, clk) * 1e3)
+    rows = []
+    for bs in (1, 16, 64):
+        s, c = statistics.median(times[(bs, False)]), statistics.median(times[(bs, True)])
+        rows.append({"block_size": bs, "scattered_us": round(s, 2), "contiguous_us": round(c, 2),
+                     "ratio": round(s / c, 4)})
+    return {"ratio_max": max(r["ratio"] for r in rows), "rows": rows, "repeats": repeats,
+            "workload": "layout B32 ctx2048, Qwen3-4B heads, bf16, block sizes 1/16/64"}
+
+
+def tensor_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))
+    return 1900.0, 1700.0
+
+
+def prefill_record():
+    """The tensor-core prefill kernel's ncu figures, if they were taken on its
+    current source."""
+    path = os.path.join(ROOT, "profiles", "prefill_tc_record.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != source_hash(PREFILL_SOURCES):
+        return None
+    return rec
+
+
 # ------------------------------------------------------------------ oracle
-def cpu_baseline(wl, nb, budget_s=20.0, nthreads=None):
+def cpu_baseline(wl, nb, budget_s=20.0, nthreads=None, single_budget_s=6.0):
     """The oracle as it stands, on the host cores: its cache is built once
     (untimed), then whole steps (slot mapping, append of the new rows,
-    attention of every row) are timed until the budget is spent."""
+    attention of every row) are timed with all the cores until the budget is
+    spent.  The same oracle on one thread is timed on a sample of the step's
+    (token, head) rows (its attention is over rows, so a sample scales to the
+    whole step by rows), with the full slot mapping and append."""
     import oracle
 
     nthreads = nthreads or oracle.cpu_count()
@@ -477,9 +699,29 @@ def cpu_baseline(wl, nb, budget_s=20.0, nthreads=None):
                          wl.v_scale, nthreads=nthreads)
         times.append(time.perf_counter() - t0)
     per = statistics.median(times)
+    # one thread: append + slot mapping in full, attention over a row sample
+    n_all = wl.T * wl.Hq
+    order = np.random.default_rng(4243).permutation(n_all)
+    t0 = time.perf_counter()
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.seq_lens, wl.block_tables, wl.block_size)
+    oracle.append(kn, vn, slots, kc, vc, wl.k_scale, wl.v_scale)
+    t_fixed = time.perf_counter() - t0
+    done, t_rows = 0, 0.0
+    while done < n_all and t_rows < single_budget_s:
+        sel = order[done:done + 64]
+        t0 = time.perf_counter()
+        oracle.attention(wl.q, wl.cu_seqlens_q, wl.seq_lens, wl.block_tables, kc, vc, wl.scale, wl.k_scale,
+                         wl.v_scale, nthreads=1, rows=(sel // wl.Hq, (sel % wl.Hq).astype(np.int32)))
+        t_rows += time.perf_counter() - t0
+        done += sel.shape[0]
+    per_1 = t_fixed + t_rows * n_all / done
     return {"value": round(nb["total"] / per / 1e9, 3), "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"{len(times)} whole steps of the same workload (all {wl.T} query rows), "
-                      f"median {per * 1e3:.1f} ms per step, fp64, {nthreads} threads"}
+                      f"median {per * 1e3:.1f} ms per step, fp64, {nthreads} threads",
+            "single_thread": {"value": round(nb["total"] / per_1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                              "ms_per_step": round(per_1 * 1e3, 1),
+                              "sample": f"{done} of {n_all} (token, head) rows on one thread, scaled to the "
+                                        f"step by rows, plus the full slot mapping and append"}}
 
 
 def make_workload(name, rank=0):
@@ -579,47 +821,64 @@ def run_reference(args, rank, world, budget_s=90.0):
 
 # ------------------------------------------------------------------ main
 def run_layout_compare(args):
-    """Scattered against contiguous block tables on the layout workloads
-    (B 32 x 2048 keys, block sizes 1, 16, 64): each repeat allocates fresh
-    caches for each layout (alternating which goes first) and times 200
-    back-to-back pkv_attention calls over 4 rotated layer caches with CUDA
-    events.  Reports per-layout medians and their ratio."""
+    """Scattered against contiguous block tables on the layout workloads, as
+    its own JSON line (see layout_ratio)."""
     import torch
-    from paged_kv_cache_mapping_gb300 import harness, pkv_device_errors
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    calls, layers = 200, 4
-    times = {}
-    for r in range(args.repeats):
-        for bs in (1, 16, 64):
-            for contiguous in ((False, True) if r % 2 == 0 else (True, False)):
-                wl = W.layout_sweep(bs, contiguous, seed=1003)
-                ds = harness.DeviceStep(wl, out_dtype=torch.bfloat16, layers=layers, max_q_len=1)
-                for i in range(max(args.warmup, 3) * layers):
-                    ds.attention_only(i % layers)
-                torch.cuda.synchronize()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                for i in range(calls):
-                    ds.attention_only(i % layers)
-                b.record()
-                torch.cuda.synchronize()
-                if pkv_device_errors(dev):
-                    raise RuntimeError("device error flags set in the layout comparison")
-                times.setdefault((bs, contiguous), []).append(a.elapsed_time(b) / calls * 1e3)
-                del ds
-                torch.cuda.empty_cache()
-    rows = []
-    for bs in (1, 16, 64):
-        s, c = statistics.median(times[(bs, False)]), statistics.median(times[(bs, True)])
-        rows.append({"block_size": bs, "scattered_us": round(s, 2), "contiguous_us": round(c, 2),
-                     "ratio": round(s / c, 4)})
-    return {"metric": "pkv_attention time, scattered / contiguous block tables", "unit": "ratio",
-            "value": max(r["ratio"] for r in rows), "higher_is_better": False, "repeats": args.repeats,
-            "config": {"workload": "layout B32 ctx2048, Qwen3-4B heads, bf16, block sizes 1/16/64",
-                       "timing": f"median over repeats of {calls} back-to-back calls, {layers} layer caches rotated"},
-            "rows": rows}
+    with ClockSampler(dev.index) as clk:
+        r = layout_ratio(dev, repeats=args.repeats, clk=clk)
+    return {"metric": "pkv_attention_run time, scattered / contiguous block tables", "unit": "ratio",
+            "value": r["ratio_max"], "higher_is_better": False, "repeats": args.repeats,
+            "config": {"workload": r["workload"],
+                       "timing": "median over repeats of 200 back-to-back runs, 4 layer caches rotated"},
+            "rows": r["rows"], "clocks": clk.summary()}
 
+
+def skew_workloads(B, mean_ctx=2048, seed=1007):
+    """Decode batches of B sequences with the same total keys (B * mean_ctx):
+    uniform (every sequence mean_ctx), one long (one sequence holds half of
+    the keys, the others share the rest) and heavy-tailed (log-normal, sigma
+    1.5, scaled to the total), at Qwen3-4B heads, bf16, block size 16."""
+    total = B * mean_ctx
+    uni = np.full(B, mean_ctx, np.int64)
+    one = np.full(B, max(1, (total - total // 2) // max(1, B - 1)), np.int64)
+    one[B // 2] = total - one.sum() + one[B // 2]
+    g = W.rng(seed, 4, B)
+    x = np.exp(g.normal(0.0, 1.5, size=B))
+    tail = np.maximum(1, np.floor(x / x.sum() * total)).astype(np.int64)
+    tail[int(np.argmax(tail))] += total - tail.sum()
+    out = {}
+    for name, lens in (("uniform", uni), ("one_long", one), ("heavy_tail", tail)):
+        assert int(lens.sum()) == total and (lens >= 1).all()
+        mb = -(-int(lens.max()) // 16)
+        out[name] = W.build(f"skew {name} B{B} total {total}", Hq=32, Hkv=8, D=128, block_size=16,
+                            seq_lens=lens.astype(np.int32), q_lens=np.ones(B, np.int32), src="bf16", kv="bf16",
+                            seed=seed + B, max_blocks=mb, pool_slack=0.02)
+    return out
+
+
+def run_skew_compare(args):
+    """Uniform against skewed batches at equal total keys, B = 4, 16, 64,
+    128: pkv_attention_run time and its ratio to the uniform batch."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rows = []
+    with ClockSampler(dev.index) as clk:
+        for B in (4, 16, 64, 128):
+            wls = skew_workloads(B)
+            t = {name: time_runs(wl, dev, 200, clk=clk) * 1e3 for name, wl in wls.items()}
+            rows.append({"batch": B, "total_keys": int(wls["uniform"].seq_lens.sum()),
+                         "max_ctx": {k: int(w.seq_lens.max()) for k, w in wls.items()},
+                         "us": {k: round(v, 2) for k, v in t.items()},
+                         "ratio_one_long": round(t["one_long"] / t["uniform"], 4),
+                         "ratio_heavy_tail": round(t["heavy_tail"] / t["uniform"], 4)})
+    return {"metric": "pkv_attention_run time, skewed / uniform batch at equal total keys", "unit": "ratio",
+            "value": max(max(r["ratio_one_long"], r["ratio_heavy_tail"]) for r in rows), "higher_is_better": False,
+            "config": {"workload": "decode, Qwen3-4B heads, bf16, block size 16, mean context 2048",
+                       "timing": "200 back-to-back runs over 4 rotated layer caches after one plan"},
+            "rows": rows, "clocks": clk.summary()}
 
 
 def main(argv=None):
@@ -632,10 +891,15 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=4, help="layer caches rotated across steps")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other workloads' keys (layout, mixed prefill, fp8)")
+    ap.add_argument("--layout-repeats", type=int, default=2, help="fresh allocations per layout in the line")
     ap.add_argument("--soft-cap", type=float, default=0.0, help="logits soft cap (variant; 0: off)")
     ap.add_argument("--window-left", type=int, default=-1, help="sliding window (variant; < 0: off)")
     ap.add_argument("--layout-compare", action="store_true",
                     help="print scattered / contiguous attention time on the layout workloads instead")
+    ap.add_argument("--skew-compare", action="store_true",
+                    help="print skewed / uniform attention time at equal total keys instead")
     ap.add_argument("--repeats", type=int, default=8, help="fresh allocations per layout (--layout-compare)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -646,6 +910,8 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N > 1 with torch.distributed.run")
     if args.layout_compare:
         line = run_layout_compare(args) if rank == 0 else None
+    elif args.skew_compare:
+        line = run_skew_compare(args) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

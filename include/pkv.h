@@ -53,12 +53,15 @@
  *
  * Kernels of this library are launched with programmatic dependent launch:
  * each may begin (and set up) while the previous kernel in the stream is
- * still running, and waits for it before touching memory, with one
- * exception: the plan kernel of pkv_attention reads cu_seqlens_q and
- * seq_lens before that wait.  This is safe whenever those arrays are final
- * when the previous kernel in the stream lets its successor start early --
- * always, when that kernel is one of this library's (none of them writes
- * the lengths) or a kernel that does not use programmatic launch itself.
+ * still running, and waits for that kernel to complete, with its writes
+ * visible, before it reads or writes any memory.  Inputs written by the
+ * previous kernel of the stream, the lengths included, are therefore safe.
+ *
+ * The library keeps, per device, the addresses of its own device variables
+ * (the error word, the static workspace), looked up at the first call on
+ * the device in the runtime's primary context.  It is not for use after
+ * cudaDeviceReset or under another context made current through the
+ * driver API.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -252,6 +255,50 @@ PKV_API pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_se
                                     const pkv_attention_variant* variant, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/*
+ * pkv_attention_plan / pkv_attention_run -- pkv_attention in two parts, so
+ * that one plan serves every layer of a model step.
+ * "How Easy Is It to Start Serving LLMs?", "3. Load balancing: keep every SM
+ * busy": the work of a decode step is planned once from the sequence
+ * lengths, kept in a fixed GPU buffer, and reused by the attention of every
+ * layer; scheduling then costs almost nothing per layer and stays
+ * CUDA-graph friendly.
+ *
+ * pkv_attention_plan reads cu_seqlens_q and seq_lens on the device (no
+ * device-to-host copy) and writes the work lists of the call into the
+ * workspace, with a record of the shapes they were made for.  Arguments as
+ * pkv_attention_ex; q's and k_cache's data are not read (only their shapes
+ * and dtypes), block_tables' contents are not read, and of variant only
+ * window_left matters (it decides which keys a decode reads).
+ *
+ * pkv_attention_run runs the attention of one layer over the plan in the
+ * workspace: arguments, results and errors as pkv_attention_ex, which is
+ * plan + run.  Between the plan and its runs the caller must keep
+ * cu_seqlens_q, seq_lens, the shapes of q, block_tables and the caches, the
+ * cache dtype, max_q_len and window_left unchanged; q, the caches' contents,
+ * the block tables' contents, out, scale, k_scale, v_scale and the soft cap
+ * may change from run to run.  A run leaves the plan intact, so runs may
+ * follow each other on the stream without limit; a new plan replaces the
+ * old one.  A run on a workspace whose plan was made for other shapes or
+ * choices does no work and records bit 16 in the device error word
+ * (pkv_device_errors); a run given other lengths than its plan's is not
+ * detected and gives unspecified rows.  Runs that share a workspace must not
+ * overlap on the GPU (keep them on one stream).  With f32 caches the plan is
+ * empty and a run is the whole call.
+ */
+PKV_API pkv_status pkv_attention_plan(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
+                                      const pkv_tensor* seq_lens, const pkv_tensor* block_tables,
+                                      const pkv_tensor* k_cache, int32_t max_q_len,
+                                      const pkv_attention_variant* variant, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+PKV_API pkv_status pkv_attention_run(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
+                                     const pkv_tensor* seq_lens, const pkv_tensor* block_tables,
+                                     const pkv_tensor* k_cache, const pkv_tensor* v_cache, float scale,
+                                     float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                                     const pkv_attention_variant* variant, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* Size of the scratch array inside the library that
  * pkv_attention_static_workspace uses on each device (16 MiB). */
 #define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
@@ -285,7 +332,9 @@ PKV_API pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_se
  *     keep such calls on one stream or order them with events.
  *   - the array's 16 MiB of device memory are reserved when the CUDA runtime
  *     loads the library's code for this call on a device (at the first call
- *     under lazy module loading).
+ *     under lazy module loading);
+ *   - the cached address is that of the device's primary context: after
+ *     cudaDeviceReset, or with another context current, it is stale.
  */
 PKV_API pkv_status pkv_attention_static_workspace(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
                                                   const pkv_tensor* seq_lens,
@@ -298,7 +347,8 @@ PKV_API pkv_status pkv_attention_static_workspace(const pkv_tensor* q, const pkv
  * pkv_device_errors -- synchronise the stream, then return (in *flags) and
  * clear the record of out-of-range indices the kernels met on the current
  * device since the last call.  Bits: 1 = slot beyond the pool, 2 = block id
- * out of range, 4 = inconsistent lengths, 8 = a bounded wait gave up.
+ * out of range, 4 = inconsistent lengths, 8 = a bounded wait gave up, 16 =
+ * an attention run found no plan for its shapes in the workspace.
  */
 PKV_API pkv_status pkv_device_errors(void* stream, uint32_t* flags);
 

@@ -12,6 +12,10 @@ Functions (same names as the C ABI):
   pkv_attention_workspace_size(q, block_tables, k_cache)
   pkv_attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache,
                 scale, out, k_scale=1.0, v_scale=1.0, max_q_len=0, workspace=None)
+  pkv_attention_plan(q, cu_seqlens_q, seq_lens, block_tables, k_cache, workspace,
+                     max_q_len=0, window_left=-1)
+  pkv_attention_run(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache,
+                    scale, out, workspace, k_scale=1.0, v_scale=1.0, max_q_len=0)
   pkv_attention_static_workspace(q, cu_seqlens_q, seq_lens, block_tables, k_cache,
                                  v_cache, scale, out, k_scale=1.0, v_scale=1.0, max_q_len=0)
   pkv_device_errors()
@@ -22,12 +26,13 @@ import os
 import torch
 
 __all__ = ["PkvError", "pkv_slot_mapping", "pkv_csr_to_block_tables", "pkv_append", "pkv_attention", "pkv_attention_workspace_size",
-           "pkv_attention_static_workspace", "pkv_device_errors", "pkv_version", "library_path", "load_library",
+           "pkv_attention_plan", "pkv_attention_run", "pkv_attention_static_workspace", "pkv_device_errors", "pkv_version", "library_path", "load_library",
            "EXPORTED", "STATIC_WORKSPACE_BYTES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpkv.so")
 EXPORTED = ("pkv_slot_mapping", "pkv_append", "pkv_attention_workspace_size", "pkv_attention", "pkv_attention_ex",
+            "pkv_attention_plan", "pkv_attention_run",
             "pkv_attention_static_workspace", "pkv_device_errors", "pkv_status_string", "pkv_last_error",
             "pkv_version", "pkv_csr_to_block_tables", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_append",
             "pkv_bm_free_sequence", "pkv_bm_block_table", "pkv_bm_build_step", "pkv_bm_stats")
@@ -84,6 +89,13 @@ def load_library():
                                          ctypes.c_int32, P, ctypes.POINTER(_Variant), ctypes.c_void_p,
                                          ctypes.c_size_t, ctypes.c_void_p]
         lib.pkv_attention_ex.restype = st
+        lib.pkv_attention_plan.argtypes = [P, P, P, P, P, ctypes.c_int32, ctypes.POINTER(_Variant), ctypes.c_void_p,
+                                           ctypes.c_size_t, ctypes.c_void_p]
+        lib.pkv_attention_plan.restype = st
+        lib.pkv_attention_run.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_int32, P, ctypes.POINTER(_Variant), ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_void_p]
+        lib.pkv_attention_run.restype = st
         lib.pkv_attention_static_workspace.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float,
                                                        ctypes.c_float, ctypes.c_int32, P, ctypes.c_void_p]
         lib.pkv_attention_static_workspace.restype = st
@@ -201,6 +213,40 @@ def pkv_attention(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, sca
     return out
 
 
+def pkv_attention_plan(q, cu_seqlens_q, seq_lens, block_tables, k_cache, workspace, max_q_len: int = 0,
+                       window_left: int = -1):
+    """Writes the work lists of an attention call into workspace, from the
+    device lengths; every later pkv_attention_run over the same lengths and
+    shapes reuses them (one plan per model step, one run per layer)."""
+    lib = load_library()
+    tq, tcu, tsl, tbt, tkc = (_tensor(q, "q"), _tensor(cu_seqlens_q, "cu_seqlens_q"), _tensor(seq_lens, "seq_lens"),
+                              _tensor(block_tables, "block_tables"), _tensor(k_cache, "k_cache"))
+    var = _Variant(0.0, int(window_left))
+    _check(lib.pkv_attention_plan(ctypes.byref(tq), ctypes.byref(tcu), ctypes.byref(tsl), ctypes.byref(tbt),
+                                  ctypes.byref(tkc), int(max_q_len), ctypes.byref(var),
+                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                  _stream(q.device)))
+
+
+def pkv_attention_run(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale: float, out, workspace,
+                      k_scale: float = 1.0, v_scale: float = 1.0, max_q_len: int = 0, soft_cap: float = 0.0,
+                      window_left: int = -1):
+    """Attention of one layer over the plan that pkv_attention_plan left in
+    workspace (same lengths, shapes, max_q_len and window_left)."""
+    lib = load_library()
+    tq, tcu, tsl, tbt, tkc, tvc, to = (
+        _tensor(q, "q"), _tensor(cu_seqlens_q, "cu_seqlens_q"), _tensor(seq_lens, "seq_lens"),
+        _tensor(block_tables, "block_tables"), _tensor(k_cache, "k_cache"), _tensor(v_cache, "v_cache"),
+        _tensor(out, "out"))
+    var = _Variant(float(soft_cap), int(window_left))
+    _check(lib.pkv_attention_run(ctypes.byref(tq), ctypes.byref(tcu), ctypes.byref(tsl), ctypes.byref(tbt),
+                                 ctypes.byref(tkc), ctypes.byref(tvc), float(scale), float(k_scale), float(v_scale),
+                                 int(max_q_len), ctypes.byref(to), ctypes.byref(var),
+                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                 _stream(q.device)))
+    return out
+
+
 def pkv_attention_static_workspace(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale: float,
                                    out, k_scale: float = 1.0, v_scale: float = 1.0, max_q_len: int = 0):
     """pkv_attention with the library's fixed per-device scratch array as the
@@ -219,7 +265,8 @@ def pkv_attention_static_workspace(q, cu_seqlens_q, seq_lens, block_tables, k_ca
 
 def pkv_device_errors(device=None) -> int:
     """Synchronises the current stream and returns (and clears) the device
-    error bits: 1 slot range, 2 block id range, 4 lengths, 8 wait timeout."""
+    error bits: 1 slot range, 2 block id range, 4 lengths, 8 wait timeout,
+    16 a run without a matching plan."""
     lib = load_library()
     flags = ctypes.c_uint32(0)
     _check(lib.pkv_device_errors(_stream(device), ctypes.byref(flags)))

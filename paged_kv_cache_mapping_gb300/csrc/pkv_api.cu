@@ -81,7 +81,7 @@ pkv_status finish(cudaStream_t st, const char* what) {
   if (flags)
     return fail(PKV_ERR_DEVICE_CHECK,
                 std::string(what) + ": device check failed, flags 0x" + std::to_string(flags) +
-                    " (1 slot range, 2 block id range, 4 lengths, 8 wait timeout)");
+                    " (1 slot range, 2 block id range, 4 lengths, 8 wait timeout, 16 no matching plan)");
   return PKV_OK;
 }
 
@@ -221,7 +221,7 @@ cudaError_t set_smem_attr(const void* kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-static int64_t max_prefill_tiles(int64_t B, int64_t T, int64_t G) {
+int64_t max_prefill_tiles(int64_t B, int64_t T, int64_t G) {
   return (T * G + kPrefillRows - 1) / kPrefillRows + B;
 }
 
@@ -425,13 +425,31 @@ pkv_status pkv_attention_workspace_size(const pkv_tensor* q, const pkv_tensor* b
 
 namespace {
 
-pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
-                          const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
-                          float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
-                          float soft_cap, int32_t window_left, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+// One attention call, validated: the kernel parameters and the choices the
+// host makes from the shapes alone.
+struct Call {
+  pkv::AttnParams p;
+  int kv;           // 0 f32, 1 bf16, 2 e4m3 caches
+  int out_kind;     // 0 f32, 1 bf16 output
+  bool prefill;     // a prefill kernel runs (max_q_len > 1, unknown, or G beyond the decode kernel)
+  bool tc;          // ... the tensor-core one
+  int64_t max_ctx;  // tokens a block table can hold
+  int sms;
+  cudaStream_t st;
+};
+
+// Validates the arguments of an attention call and fills c.  The plan call
+// passes no v_cache and no out (NULL): it needs only the shapes, the lengths
+// and the workspace.
+pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                   const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                   float scale, float k_scale, float v_scale, int32_t max_q_len, const pkv_tensor* out,
+                   float soft_cap, int32_t window_left, void* workspace, size_t workspace_bytes, void* stream,
+                   Call& c) {
+  const bool plan_only = out == nullptr;
+  if (plan_only) v_cache = k_cache;
   PKV_TRY(check_tensor("q", q, 3));
-  PKV_TRY(check_tensor("out", out, 3));
+  if (!plan_only) PKV_TRY(check_tensor("out", out, 3));
   PKV_TRY(check_tensor("seq_lens", seq_lens, 1));
   const int64_t B = seq_lens->shape[0];
   PKV_TRY(need(B <= (1 << 24), "B beyond 2^24 sequences"));
@@ -443,9 +461,11 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
   const int64_t NB = k_cache->shape[0], bs = k_cache->shape[1], Hkv = k_cache->shape[2];
   PKV_TRY(need(k_cache->shape[3] == D, "q and cache head dims differ"));
   PKV_TRY(need(Hq >= 1 && Hq % Hkv == 0, "Hq must be a positive multiple of Hkv"));
-  PKV_TRY(need(out->shape[0] == T && out->shape[1] == Hq && out->shape[2] == D, describe("out", out) +
-                                                                                     " must have q's shape"));
-  PKV_TRY(need(out->dtype == PKV_F32 || out->dtype == PKV_BF16, "out must be f32 or bf16"));
+  if (!plan_only) {
+    PKV_TRY(need(out->shape[0] == T && out->shape[1] == Hq && out->shape[2] == D,
+                 describe("out", out) + " must have q's shape"));
+    PKV_TRY(need(out->dtype == PKV_F32 || out->dtype == PKV_BF16, "out must be f32 or bf16"));
+  }
   PKV_TRY(need(block_tables->shape[1] * bs <= INT32_MAX, "max_blocks * block_size beyond int32"));
   PKV_TRY(need(T <= INT32_MAX, "T beyond int32"));
   if (NB * bs > INT32_MAX)
@@ -465,16 +485,19 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
   else if (D != 64 && D != 128)
     return fail(PKV_ERR_UNSUPPORTED, "bf16/fp8 attention is built for D = 64 and D = 128");
   PKV_TRY(need(q->stride[2] == 1 || D == 1, "q must have unit stride in D"));
-  PKV_TRY(need(out->stride[2] == 1 || D == 1, "out must have unit stride in D"));
-  const int qes = esize(q->dtype), oes = esize(out->dtype);
+  const int qes = esize(q->dtype);
   PKV_TRY(need(aligned(q->data, 16) && (q->stride[0] * qes) % 16 == 0 && (q->stride[1] * qes) % 16 == 0,
                "q rows must be 16-byte aligned (data and strides)"));
-  PKV_TRY(need(aligned(out->data, 16) && (out->stride[0] * oes) % 8 == 0 && (out->stride[1] * oes) % 8 == 0,
-               "out rows must be 8-byte aligned (data and strides)"));
-  if (kv == 2)
-    PKV_TRY(need(k_scale > 0.f && v_scale > 0.f && k_scale == k_scale && v_scale == v_scale,
-                 "fp8 scales must be positive and finite"));
-  PKV_TRY(need(scale == scale, "scale is NaN"));
+  if (!plan_only) {
+    PKV_TRY(need(out->stride[2] == 1 || D == 1, "out must have unit stride in D"));
+    const int oes = esize(out->dtype);
+    PKV_TRY(need(aligned(out->data, 16) && (out->stride[0] * oes) % 8 == 0 && (out->stride[1] * oes) % 8 == 0,
+                 "out rows must be 8-byte aligned (data and strides)"));
+    if (kv == 2)
+      PKV_TRY(need(k_scale > 0.f && v_scale > 0.f && k_scale == k_scale && v_scale == v_scale,
+                   "fp8 scales must be positive and finite"));
+    PKV_TRY(need(scale == scale, "scale is NaN"));
+  }
   const int64_t max_ctx = block_tables->shape[1] * bs;
   const size_t ws_need = pkv::attention_workspace_bytes(B, T, Hq, Hkv, D, max_ctx);
   if (kv != 0) {
@@ -483,20 +506,20 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
                                                    std::to_string(workspace_bytes));
     PKV_TRY(need(workspace != nullptr && aligned(workspace, 256), "workspace must be 256-byte aligned"));
   }
-  unsigned int* err = nullptr;
-  int sms = 0;
-  PKV_TRY(device_state(&err, &sms));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (T == 0 || B == 0) return PKV_OK;
+  c.st = static_cast<cudaStream_t>(stream);
+  c.kv = kv;
+  c.out_kind = !plan_only && out->dtype == PKV_BF16 ? 1 : 0;
+  c.max_ctx = max_ctx;
 
-  pkv::AttnParams p{};
+  pkv::AttnParams& p = c.p;
+  p = pkv::AttnParams{};
   p.q = q->data;
   p.q_st = q->stride[0];
   p.q_sh = q->stride[1];
-  p.out = out->data;
+  p.out = plan_only ? nullptr : out->data;
   p.T = T;
-  p.o_st = out->stride[0];
-  p.o_sh = out->stride[1];
+  p.o_st = plan_only ? 0 : out->stride[0];
+  p.o_sh = plan_only ? 0 : out->stride[1];
   p.cu_q = static_cast<const int32_t*>(cu_seqlens_q->data);
   p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
   p.bt = static_cast<const int32_t*>(block_tables->data);
@@ -520,15 +543,11 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
   p.window_left = window_left >= 0 ? window_left : -1;
   p.v_scale = kv == 2 ? v_scale : 1.0f;
   p.decode_max_g = 8;
-  p.err = err;
-  const int out_kind = out->dtype == PKV_BF16 ? 1 : 0;
-  cudaError_t e;
   if (kv == 0) {
     if (p.soft_cap > 0.f || p.window_left >= 0)
       return fail(PKV_ERR_UNSUPPORTED, "a soft cap or sliding window is built for bf16 and e4m3 caches");
-    e = pkv::launch_f32(p, out_kind, T, st);
-    if (e != cudaSuccess) return cuda_fail(e, "f32 attention launch");
-    return finish(st, "pkv_attention");
+    c.prefill = c.tc = false;
+    return device_state(&p.err, &c.sms);
   }
   // workspace carve-up
   {
@@ -539,6 +558,9 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
     p.ws.work = reinterpret_cast<int32_t*>(w + L.work);
     p.ws.n_merge = p.ws.work + 1;
     p.ws.pf_work = p.ws.work + 2;
+    p.ws.dec_exit = p.ws.work + 3;
+    p.ws.pf_exit = p.ws.work + 4;
+    p.ws.sig = p.ws.work + 8;
     p.ws.merge_list = reinterpret_cast<int32_t*>(w + L.merge_list);
     p.ws.done = reinterpret_cast<int32_t*>(w + L.done);
     p.ws.dec_desc = reinterpret_cast<pkv::DecodeDesc*>(w + L.dec_desc);
@@ -547,31 +569,65 @@ pkv_status attention_impl(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, c
     p.ws.part_lse = reinterpret_cast<float*>(w + L.part_lse);
   }
   const int G = p.G;
-  const bool prefill = (max_q_len > 1) || (max_q_len <= 0 && T >= 2) || G > p.decode_max_g;
-  const bool tc = prefill && pkv::prefill_tc_supported(kv, D, bs, G);
+  c.prefill = (max_q_len > 1) || (max_q_len <= 0 && T >= 2) || G > p.decode_max_g;
+  c.tc = c.prefill && pkv::prefill_tc_supported(kv, D, bs, G);
   const bool variant = p.soft_cap > 0.f || p.window_left >= 0;
-  if (variant && prefill && !tc)
+  if (variant && c.prefill && !c.tc)
     return fail(PKV_ERR_UNSUPPORTED, "a soft cap or sliding window needs decode rows, or prefill rows on bf16 "
                                      "caches with block sizes a multiple of 16 (max_q_len > 1 here)");
-  p.pf_tq = tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
-  e = pkv::launch_plan(p, st);
+  p.pf_tq = c.tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
+  p.path = !c.prefill ? 0 : (c.tc ? 2 : 1);
+  // every argument is valid: the device's error word and SM count
+  return device_state(&p.err, &c.sms);
+}
+
+pkv_status launch_plan(const Call& c) {
+  if (c.kv == 0 || c.p.T == 0 || c.p.B == 0) return PKV_OK;
+  cudaError_t e = pkv::launch_plan(c.p, c.st);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-  if (prefill) {
-    const int64_t tiles = pkv::max_prefill_tiles(B, T, G);
-    e = tc ? pkv::launch_prefill_tc(p, out_kind, tiles * Hkv, sms, st)
-           : pkv::launch_prefill(p, kv, out_kind, tiles * Hkv, sms, st);
+  return PKV_OK;
+}
+
+// The kernels of one run over the plan in the workspace: the prefill kernel
+// (if any), then the decode kernel.
+pkv_status launch_run(const Call& c) {
+  const pkv::AttnParams& p = c.p;
+  if (p.T == 0 || p.B == 0) return PKV_OK;
+  cudaError_t e;
+  if (c.kv == 0) {
+    e = pkv::launch_f32(p, c.out_kind, p.T, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "f32 attention launch");
+    return PKV_OK;
+  }
+  if (c.prefill) {
+    const int64_t tiles = pkv::max_prefill_tiles(p.B, p.T, p.G);
+    e = c.tc ? pkv::launch_prefill_tc(p, c.out_kind, tiles * p.Hkv, c.sms, c.st)
+             : pkv::launch_prefill(p, c.kv, c.out_kind, tiles * p.Hkv, c.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
-  if (G <= p.decode_max_g) {
-    const int64_t dec_seqs = std::min<int64_t>(B, T);
-    // right after the plan the decode kernel may overlap its start with the
-    // plan's end (it waits for the plan's lists on the device)
-    // programmatic launch after the plan, and after the tensor-core prefill
-    // (which waits for the plan itself); the mma.sync prefill is a plain launch
-    e = pkv::launch_decode(p, kv, out_kind, dec_seqs * pkv::max_chunks_for(max_ctx) * Hkv, sms, st, !prefill || tc);
+  if (p.G <= p.decode_max_g) {
+    const int64_t dec_seqs = std::min<int64_t>(p.B, p.T);
+    // programmatic launch after the plan or the previous kernel of the
+    // stream, and after the tensor-core prefill (the decode kernel waits for
+    // its predecessor before reading anything); after the mma.sync prefill
+    // it is a plain launch
+    e = pkv::launch_decode(p, c.kv, c.out_kind, dec_seqs * pkv::max_chunks_for(c.max_ctx) * p.Hkv, c.sms, c.st,
+                           !c.prefill || c.tc);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
-  return finish(st, "pkv_attention");
+  return PKV_OK;
+}
+
+pkv_status variant_args(const pkv_attention_variant* variant, float& cap, int32_t& window) {
+  cap = 0.f;
+  window = -1;
+  if (variant != nullptr) {
+    PKV_TRY(need(variant->logits_soft_cap >= 0.f && variant->logits_soft_cap < INFINITY,
+                 "logits_soft_cap must be finite and >= 0 (0: off)"));
+    cap = variant->logits_soft_cap;
+    window = variant->window_left < 0 ? -1 : variant->window_left;
+  }
+  return PKV_OK;
 }
 
 }  // namespace
@@ -582,8 +638,8 @@ pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, co
                          const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
                          float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  return attention_impl(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale,
-                        max_q_len, out, 0.f, -1, workspace, workspace_bytes, stream);
+  return pkv_attention_ex(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale,
+                          max_q_len, out, nullptr, workspace, workspace_bytes, stream);
 }
 
 pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
@@ -591,16 +647,46 @@ pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q,
                             float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
                             const pkv_attention_variant* variant, void* workspace, size_t workspace_bytes,
                             void* stream) {
-  float cap = 0.f;
-  int32_t window = -1;
-  if (variant != nullptr) {
-    PKV_TRY(need(variant->logits_soft_cap >= 0.f && variant->logits_soft_cap < INFINITY,
-                 "logits_soft_cap must be finite and >= 0 (0: off)"));
-    cap = variant->logits_soft_cap;
-    window = variant->window_left < 0 ? -1 : variant->window_left;
-  }
-  return attention_impl(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale,
-                        max_q_len, out, cap, window, workspace, workspace_bytes, stream);
+  float cap;
+  int32_t window;
+  PKV_TRY(variant_args(variant, cap, window));
+  PKV_TRY(need(out != nullptr, "out is NULL"));
+  Call c;
+  PKV_TRY(prepare(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale, max_q_len,
+                  out, cap, window, workspace, workspace_bytes, stream, c));
+  PKV_TRY(launch_plan(c));
+  PKV_TRY(launch_run(c));
+  return finish(c.st, "pkv_attention");
+}
+
+pkv_status pkv_attention_plan(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                              const pkv_tensor* block_tables, const pkv_tensor* k_cache, int32_t max_q_len,
+                              const pkv_attention_variant* variant, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  float cap;
+  int32_t window;
+  PKV_TRY(variant_args(variant, cap, window));
+  Call c;
+  PKV_TRY(prepare(q, cu_seqlens_q, seq_lens, block_tables, k_cache, nullptr, 1.f, 1.f, 1.f, max_q_len, nullptr,
+                  cap, window, workspace, workspace_bytes, stream, c));
+  PKV_TRY(launch_plan(c));
+  return finish(c.st, "pkv_attention_plan");
+}
+
+pkv_status pkv_attention_run(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pkv_tensor* seq_lens,
+                             const pkv_tensor* block_tables, const pkv_tensor* k_cache, const pkv_tensor* v_cache,
+                             float scale, float k_scale, float v_scale, int32_t max_q_len, pkv_tensor* out,
+                             const pkv_attention_variant* variant, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  float cap;
+  int32_t window;
+  PKV_TRY(variant_args(variant, cap, window));
+  PKV_TRY(need(out != nullptr, "out is NULL"));
+  Call c;
+  PKV_TRY(prepare(q, cu_seqlens_q, seq_lens, block_tables, k_cache, v_cache, scale, k_scale, v_scale, max_q_len,
+                  out, cap, window, workspace, workspace_bytes, stream, c));
+  PKV_TRY(launch_run(c));
+  return finish(c.st, "pkv_attention_run");
 }
 
 }  // extern "C"

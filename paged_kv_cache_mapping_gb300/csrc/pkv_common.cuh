@@ -19,6 +19,7 @@ enum : unsigned int {
   kErrBlockRange = 2u,   // block id outside [0, num_blocks)
   kErrLengths = 4u,      // q_s < 0, q_s > N_s or N_s beyond the block table
   kErrWaitTimeout = 8u,  // a bounded wait gave up
+  kErrPlan = 16u,        // the workspace holds no plan for this call's shapes
 };
 
 // A bounded wait gives up after this many SM clock cycles (about 2 s).

@@ -176,7 +176,7 @@ struct ItemMeta {
 };
 
 template <int KV, int D, typename OutT>
-__global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(AttnParams p) {
+__device__ __forceinline__ void decode_body(const AttnParams& p) {
   using Geo = DecodeGeom<KV, D>;
   constexpr int RowB = Geo::kRowB, ST = Geo::kST, MT = Geo::kMT, QRowB = Geo::kQRowB;
   const int HP = p.hp, NS = p.ns, G = p.G;
@@ -214,6 +214,10 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
   }
   __syncthreads();
   grid_dep_wait();  // the plan kernel's lists are complete from here on
+  if (!plan_matches(p)) {  // the same answer in every thread
+    if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
+    return;
+  }
   if (warp > HP + 1) return;  // launched with (HP + 2) warps; nothing else to do
   const int HG = p.Hkv / HP;
   // a merge is cut into G parts of HP query heads (one per consumer warp),
@@ -677,6 +681,22 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
     if (++islot == 2) {
       islot = 0;
       iphase ^= 1;
+    }
+  }
+}
+
+template <int KV, int D, typename OutT>
+__global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(AttnParams p) {
+  decode_body<KV, D, OutT>(p);
+  // every warp of the CTA is done with the counters; the last CTA of the
+  // grid leaves them reset for the next run over the same plan (a run
+  // without a matching plan writes nothing; the test has one answer for
+  // the whole grid)
+  if (plan_matches(p) && last_cta_of_grid(p.ws.dec_exit)) {
+    for (int i = threadIdx.x; i < p.B * p.Hkv; i += blockDim.x) p.ws.done[i] = 0;
+    if (threadIdx.x == 0) {
+      *p.ws.work = 0;
+      *p.ws.dec_exit = 0;
     }
   }
 }

@@ -70,6 +70,9 @@ struct Workspace {
   int32_t* work;         // [1] next decode item to hand out
   int32_t* n_merge;      // [1] sequences split into more than one chunk
   int32_t* pf_work;      // [1] next tensor-core prefill unit to hand out
+  int32_t* dec_exit;     // [1] decode CTAs finished (the last one resets the decode counters)
+  int32_t* pf_exit;      // [1] tensor-core prefill CTAs finished (the last one resets pf_work)
+  int32_t* sig;          // [kPlanSig] what the plan was made for (plan_signature)
   int32_t* merge_list;   // [B] those sequences
   int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group)
   DecodeDesc* dec_desc;  // [B * max_chunks] decode work: full chunks first, then ragged tails
@@ -105,6 +108,7 @@ struct AttnParams {
   int32_t hp;            // decode: KV heads per work item (consumer warps), divides Hkv, <= 8
   int32_t ns;            // decode: stages in the staging ring
   int32_t pf_tq;         // tensor-core prefill: query tokens per tile (0: the mma.sync prefill tiles)
+  int32_t path;          // prefill kernel of the call: 0 none, 1 mma.sync, 2 tensor-core (tcgen05)
   // variants: soft_cap > 0 turns a score s into soft_cap * tanh(s / soft_cap);
   // the kernels take x = cap_post * tanh(raw * cap_pre) in base 2, raw being
   // the q.k dot product of the stored values.  window_left >= 0: the query
@@ -114,6 +118,53 @@ struct AttnParams {
   Workspace ws;
   unsigned int* err;
 };
+
+// The shapes and choices a plan depends on, written by the plan kernel into
+// the workspace and checked by every kernel of a run before it reads the
+// plan's lists: a run whose call disagrees with the plan in the workspace
+// does no work and records kErrPlan.
+constexpr int kPlanSig = 12;
+constexpr int32_t kPlanMagic = 0x504b5631;  // "PKV1"
+__host__ __device__ inline void plan_signature(const AttnParams& p, int32_t (&sig)[kPlanSig]) {
+  sig[0] = kPlanMagic;
+  sig[1] = p.B;
+  sig[2] = static_cast<int32_t>(p.T);
+  sig[3] = p.Hkv;
+  sig[4] = p.G;
+  sig[5] = p.D;
+  sig[6] = p.bs;
+  sig[7] = p.max_blocks;
+  sig[8] = p.pf_tq;
+  sig[9] = p.path;
+  sig[10] = p.window_left;
+  sig[11] = p.decode_max_g;
+}
+
+// Every thread of a run kernel may call this after its dependency wait (the
+// signature is written by the plan kernel and not changed by a run).
+__device__ __forceinline__ bool plan_matches(const AttnParams& p) {
+  int32_t want[kPlanSig];
+  plan_signature(p, want);
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < kPlanSig; ++i) ok &= __ldcg(p.ws.sig + i) == want[i];
+  return ok;
+}
+
+// Called by every thread of a run kernel at its end: true in the last CTA
+// of the grid to get there, after all the others have finished with the
+// run's counters (each CTA fences its own accesses before it reports).
+__device__ __forceinline__ bool last_cta_of_grid(int32_t* exit_count) {
+  __shared__ int last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(exit_count, 1) == static_cast<int>(gridDim.x) - 1;
+    __threadfence();
+  }
+  __syncthreads();
+  return last != 0;
+}
 
 // Launchers.  out_kind: 0 = f32, 1 = bf16.  kv: 0 = f32, 1 = bf16, 2 = e4m3.
 // Prefill tiles of a call are at most ceil(T * G / 64) + B; decode chunks at

@@ -68,9 +68,10 @@ struct SeqCounts {
 };
 
 __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool record) {
-  const int c0 = __ldg(p.cu_q + s), c1 = __ldg(p.cu_q + s + 1);
+  // L2 loads: the lengths may have been written by the previous kernel
+  const int c0 = __ldcg(p.cu_q + s), c1 = __ldcg(p.cu_q + s + 1);
   const int q_s = c1 - c0;
-  const int n = __ldg(p.seq_lens + s);
+  const int n = __ldcg(p.seq_lens + s);
   SeqCounts c{0, 0, 0, 0, n, c0, q_s};
   if (q_s == 0) return c;
   if (q_s < 0 || q_s > n || (int64_t)n > (int64_t)p.max_blocks * p.bs || c0 < 0 || c1 > p.T) {
@@ -125,17 +126,21 @@ constexpr int kPlanSeqs = 512;
 // One block: per-sequence work counts and their prefix sums, the decode
 // work list (every full chunk first, then the ragged last chunks, so that
 // the small pieces come last), the list of split sequences, the prefill
-// tile list, and the per-call counters reset.  Reads device lengths; no
-// host round trip.
+// tile list, the counters of the run kernels reset, and the plan's
+// signature.  Reads device lengths; no host round trip.  A plan serves any
+// number of runs (one per layer) over the same lengths: each run's kernels
+// leave their counters reset when they finish.
 __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
-  launch_dependents();  // the decode kernel may start its set-up now
+  launch_dependents();  // the next kernel may start its set-up now
+  // launched with programmatic dependent launch: the lengths may come from
+  // the previous kernel, and the workspace may still be read by the previous
+  // run's kernels until that kernel has completed
+  grid_dep_wait();
   const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
   const int B = p.B;
   const int per = (B + nth - 1) / nth;
   const int s0 = min(tid * per, B), s1 = min(s0 + per, B);
-  // First pass, counts and their prefix sums.  It reads only the lengths,
-  // which no kernel of this library writes, so it runs before the wait
-  // below, while the previous kernel (e.g. the append) is still running.
+  // First pass, counts and their prefix sums.
   SeqCounts first{};  // the thread's first sequence, kept for the second pass
   int sum[5] = {0, 0, 0, 0, 0};
   for (int s = s0; s < s1; ++s) {
@@ -149,10 +154,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   }
   int off[5], tot[5];
   block_scan<5>(sum, off, tot);
-  // launched with programmatic dependent launch: the workspace may still be
-  // read by the previous attention call's kernels until the previous kernel
-  // has completed
-  grid_dep_wait();
   __shared__ int4 sq_cnt[kPlanSeqs];  // dec, full, pf, n
   __shared__ int4 sq_off[kPlanSeqs];  // off[0..3]
   __shared__ int2 sq_len[kPlanSeqs];  // t0, q_s
@@ -191,7 +192,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     p.ws.pf_off[B] = tot[3];
     *p.ws.work = 0;
     *p.ws.pf_work = 0;
+    *p.ws.dec_exit = 0;
+    *p.ws.pf_exit = 0;
     *p.ws.n_merge = tot[4];
+  }
+  if (tid < kPlanSig) {
+    int32_t sig[kPlanSig];
+    plan_signature(p, sig);
+    p.ws.sig[tid] = sig[tid];
   }
   for (int i = tid; i < B * p.Hkv; i += nth) p.ws.done[i] = 0;
 }

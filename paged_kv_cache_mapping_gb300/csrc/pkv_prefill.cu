@@ -61,6 +61,10 @@ template <int KV, int D, typename OutT>
 __global__ void __launch_bounds__(PrefillCfg<KV, D>::kThreads, 2) prefill_kernel(AttnParams p) {
   using C = PrefillCfg<KV, D>;
   using R = Ring<C::kRowB, C::kRowS, C::kST, C::kNS>;
+  if (!plan_matches(p)) {  // the same answer in every thread
+    if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
+    return;
+  }
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)C::kNS * C::kStageB);
   volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * C::kNS);  // [0] abort

@@ -198,15 +198,9 @@ __device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigne
 // the CTA's units (g); tile g uses K/V stage g % 3 and S / P buffer g % 2,
 // and signals o_done[g % 2] when its P V has finished.
 template <int D, typename OutT>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+__device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                                const CUtensorMap& tm_v) {
   using Geo = TcGeom<D>;
-  // launched with programmatic dependent launch right after the plan: wait
-  // for its lists (every thread, before any global access), then let the
-  // decode kernel that follows launch and set up on the SMs this grid frees
-  grid_dep_wait();
-  launch_dependents();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sQ = smem_u32(smem + Geo::kOffQ);
@@ -689,6 +683,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Geo::kTmemCols));
+  }
+}
+
+template <int D, typename OutT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  // launched with programmatic dependent launch: wait for the previous
+  // kernel (every thread, before any global access), then let the decode
+  // kernel that follows launch and set up on the SMs this grid frees
+  grid_dep_wait();
+  launch_dependents();
+  const bool planned = plan_matches(p);  // one answer for the whole grid
+  if (planned)
+    prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v);
+  else if (threadIdx.x == 0)
+    atomicOr(p.err, kErrPlan);
+  // the last CTA leaves the unit counter reset for the next run of the plan
+  if (planned && last_cta_of_grid(p.ws.pf_exit) && threadIdx.x == 0) {
+    *p.ws.pf_work = 0;
+    *p.ws.pf_exit = 0;
   }
 }
 

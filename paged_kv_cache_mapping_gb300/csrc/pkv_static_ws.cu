@@ -17,6 +17,11 @@
 //
 // Calls whose GPU work can overlap (different streams, or host threads
 // without ordering between them) share the one array and race on it.
+//
+// The cached address belongs to the context that was current at the first
+// call on the device: the device's primary context, which the CUDA runtime
+// uses.  After cudaDeviceReset, or under another context made current with
+// the driver API, that address is stale; the call is not for such use.
 #include <mutex>
 #include <string>
 
@@ -63,6 +68,12 @@ extern "C" pkv_status pkv_attention_static_workspace(const pkv_tensor* q, const 
                                                      const pkv_tensor* k_cache, const pkv_tensor* v_cache,
                                                      float scale, float k_scale, float v_scale,
                                                      int32_t max_q_len, pkv_tensor* out, void* stream) {
+  // the batch the call would run is seq_lens' B; a block table of another
+  // height is the argument error pkv_attention reports, not a size error
+  if (seq_lens == nullptr || seq_lens->ndim != 1 || block_tables == nullptr || block_tables->ndim != 2 ||
+      block_tables->shape[0] != seq_lens->shape[0])
+    return pkv::record_failure(PKV_ERR_INVALID_ARGUMENT,
+                               "pkv_attention_static_workspace: seq_lens must be [B] and block_tables [B, max_blocks]");
   size_t need = 0;
   pkv_status st = pkv_attention_workspace_size(q, block_tables, k_cache, &need);
   if (st != PKV_OK) return st;
@@ -70,7 +81,7 @@ extern "C" pkv_status pkv_attention_static_workspace(const pkv_tensor* q, const 
     return pkv::record_failure(
         PKV_ERR_WORKSPACE_TOO_SMALL,
         "pkv_attention_static_workspace: this call needs " + std::to_string(need) +
-            " bytes of scratch (B = " + std::to_string(block_tables->shape[0]) +
+            " bytes of scratch (B = " + std::to_string(seq_lens->shape[0]) +
             ", T = " + std::to_string(q->shape[0]) + ", Hq = " + std::to_string(q->shape[1]) +
             ", max context = " + std::to_string(block_tables->shape[1] * k_cache->shape[1]) +
             " tokens) but the library's static array holds " + std::to_string(PKV_STATIC_WORKSPACE_BYTES) +

@@ -8,7 +8,8 @@ every query row.  Used by the benchmark, the smoke check and the GPU tests.
 import numpy as np
 import torch
 
-from . import pkv_append, pkv_attention, pkv_attention_workspace_size, pkv_slot_mapping
+from . import (pkv_append, pkv_attention, pkv_attention_plan, pkv_attention_run, pkv_attention_workspace_size,
+               pkv_slot_mapping)
 from .workloads import Workload
 
 CACHE_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
@@ -95,3 +96,32 @@ class DeviceStep:
                       self.out if out is None else out, wl.k_scale, wl.v_scale, self.max_q_len, self.ws,
                       soft_cap=self.soft_cap, window_left=self.window_left)
         return self.out if out is None else out
+
+    # ---- one plan per model step, one run per layer
+    def plan(self):
+        """The work lists of this step's lengths, into the workspace."""
+        pkv_attention_plan(self.q, self.cu_q, self.seq_lens, self.bt, self.caches[0][0], self.ws,
+                           max_q_len=self.max_q_len, window_left=self.window_left)
+
+    def run(self, layer: int = 0, out=None, q=None):
+        """Attention of one layer over the plan in the workspace."""
+        wl = self.wl
+        kc, vc = self.caches[layer]
+        out = self.out if out is None else out
+        pkv_attention_run(self.q if q is None else q, self.cu_q, self.seq_lens, self.bt, kc, vc, wl.scale, out,
+                          self.ws, wl.k_scale, wl.v_scale, self.max_q_len, soft_cap=self.soft_cap,
+                          window_left=self.window_left)
+        return out
+
+    def layer_step(self, layer: int = 0, out=None):
+        """The per-layer part of a model step whose slots and plan are
+        already made: append of the layer's new rows, then attention."""
+        wl = self.wl
+        kc, vc = self.caches[layer]
+        pkv_append(self.k_new, self.v_new, self.slots, kc, vc, wl.k_scale, wl.v_scale)
+        return self.run(layer, out)
+
+    def model_step_start(self):
+        """The per-step part: slot mapping of the new rows and the plan."""
+        pkv_slot_mapping(self.cu_q, self.seq_lens, self.bt, self.wl.block_size, out=self.slots)
+        self.plan()

@@ -13,9 +13,10 @@ from tests.helpers import rel_l2
 # attention path (bf16 inputs, fp32 accumulation and output).  fp8
 # caches: max |err| <= 1e-2 against the oracle on the same dequantised
 # values.  fp32 everything: the kernel accumulates in fp32 (unit roundoff
-# 6e-8) over at most a few hundred terms per dot product and sum, so 1e-5
-# absolute / 1e-5 relative L2 leaves a wide margin over the rounding.
-TOL = {"bf16": (2e-3, 1e-3), "e4m3": (1e-2, 1e-2), "f32": (1e-5, 1e-5)}
+# 6e-8) over at most a few hundred terms per dot product and sum; the tiny
+# fp32 workload measures about 1e-7 relative L2, so 1e-5 absolute and 1e-6
+# relative L2 keep a margin of ten over the rounding.
+TOL = {"bf16": (2e-3, 1e-3), "e4m3": (1e-2, 1e-2), "f32": (1e-5, 1e-6)}
 
 
 def run_gpu(wl, out_dtype=torch.float32, **kw):

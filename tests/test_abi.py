@@ -157,3 +157,27 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(pkv.PkvError):
         pkv.pkv_slot_mapping(torch.zeros(5, dtype=torch.int32), torch.zeros(4, dtype=torch.int32),
                              torch.zeros(4, 4, dtype=torch.int32), 16, T=4)
+
+
+def test_plan_and_run_validation(lib):
+    """The split call checks its arguments on the host like pkv_attention:
+    a short workspace, mismatched shapes and a variant the prefill kernel in
+    use cannot take are refused before any launch."""
+    r = ctypes.byref
+    a = good()
+    ws = ctypes.c_void_p(FAKE)
+    args = (r(a["q"]), r(a["cu"]), r(a["sl"]), r(a["bt"]), r(a["kc"]))
+    assert lib.pkv_attention_plan(*args, 0, None, ws, 100, None) == 3
+    assert lib.pkv_attention_plan(r(a["q"]), r(_t(FAKE, I32, [4])), r(a["sl"]), r(a["bt"]), r(a["kc"]), 0, None,
+                                  ws, 1 << 30, None) == 1
+    assert lib.pkv_attention_run(*args, r(a["vc"]), 0.1, 1.0, 1.0, 0, r(a["out"]), None, ws, 100, None) == 3
+    assert lib.pkv_attention_run(*args, r(a["vc"]), 0.1, 1.0, 1.0, 0, r(_t(FAKE, F32, [4, 32, 64])), None, ws,
+                                 1 << 30, None) == 1
+    assert lib.pkv_attention_run(*args, r(a["vc"]), 0.1, 1.0, 1.0, 0, None, None, ws, 1 << 30, None) == 1
+    # a window on e4m3 caches with prefill rows (mma.sync prefill): unsupported, plan and run alike
+    b = good(kdt=E4M3)
+    var = pkv._Variant(0.0, 64)
+    assert lib.pkv_attention_plan(r(b["q"]), r(b["cu"]), r(b["sl"]), r(b["bt"]), r(b["kc"]), 8, r(var), ws,
+                                  1 << 30, None) == 2
+    assert lib.pkv_attention_run(r(b["q"]), r(b["cu"]), r(b["sl"]), r(b["bt"]), r(b["kc"]), r(b["vc"]), 0.1, 1.0,
+                                 1.0, 8, r(b["out"]), r(var), ws, 1 << 30, None) == 2

@@ -86,10 +86,12 @@ def test_static_workspace_matches_caller_workspace_over_consecutive_calls():
                                            wl.k_scale, wl.v_scale, ds.max_q_len)
         torch.cuda.synchronize()
         assert pkv.pkv_device_errors() == 0, name
-        ref = expected[name].double()
-        got = out.double()
-        assert torch.isfinite(got).all(), name
-        tol_abs, tol_rel = TOL[wl.kv]
-        err = (got - ref).abs().max().item()
-        rel = ((got - ref).norm() / ref.norm().clamp_min(1e-30)).item()
-        assert err <= tol_abs and rel <= tol_rel, f"{name}: max |err| {err:.3e}, rel L2 {rel:.3e}"
+        # the same kernels on the same inputs with a plan that depends only on
+        # the lengths: the results must be the same bits; the tolerance is
+        # reported only to make a failure easier to read
+        if not torch.equal(out, expected[name]):
+            ref, got = expected[name].double(), out.double()
+            err = (got - ref).abs().max().item()
+            tol_abs, tol_rel = TOL[wl.kv]
+            raise AssertionError(f"{name}: static-array result differs from the caller-workspace result "
+                                 f"(max |diff| {err:.3e}; attention tolerance {tol_abs})")
