@@ -282,7 +282,9 @@ PKV_API pkv_status pkv_attention_ex(const pkv_tensor* q, const pkv_tensor* cu_se
  * old one.  A run on a workspace whose plan was made for other shapes or
  * choices does no work and records bit 16 in the device error word
  * (pkv_device_errors); a run given other lengths than its plan's is not
- * detected and gives unspecified rows.  Runs that share a workspace must not
+ * detected and gives unspecified rows.  The runs of a plan keep count of
+ * the work they claim in the workspace; after a run that recorded a wait
+ * timeout (bit 8) those counts are off, so make a new plan.  Runs that share a workspace must not
  * overlap on the GPU (keep them on one stream).  With f32 caches the plan is
  * empty and a run is the whole call.
  */

@@ -236,7 +236,7 @@ static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t
   size_t n = 0;
   L.dec_off = n;  n += align_up(sizeof(int32_t) * (B + 1), 256);
   L.pf_off = n;   n += align_up(sizeof(int32_t) * (B + 1), 256);
-  L.work = n;     n += 256;  // decode work counter, merge count, prefill work counter
+  L.work = n;     n += 256;  // claim counters, merge count, plan signature
   L.merge_list = n; n += align_up(sizeof(int32_t) * B, 256);
   L.done = n;     n += align_up(sizeof(int32_t) * B * Hkv, 256);
   L.dec_desc = n; n += align_up(sizeof(DecodeDesc) * units, 256);
@@ -555,12 +555,10 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
     char* w = static_cast<char*>(workspace);
     p.ws.dec_off = reinterpret_cast<int32_t*>(w + L.dec_off);
     p.ws.pf_off = reinterpret_cast<int32_t*>(w + L.pf_off);
-    p.ws.work = reinterpret_cast<int32_t*>(w + L.work);
-    p.ws.n_merge = p.ws.work + 1;
-    p.ws.pf_work = p.ws.work + 2;
-    p.ws.dec_exit = p.ws.work + 3;
-    p.ws.pf_exit = p.ws.work + 4;
-    p.ws.sig = p.ws.work + 8;
+    p.ws.work = reinterpret_cast<unsigned long long*>(w + L.work);
+    p.ws.pf_work = p.ws.work + 1;
+    p.ws.n_merge = reinterpret_cast<int32_t*>(w + L.work + 16);
+    p.ws.sig = reinterpret_cast<int32_t*>(w + L.work + 32);
     p.ws.merge_list = reinterpret_cast<int32_t*>(w + L.merge_list);
     p.ws.done = reinterpret_cast<int32_t*>(w + L.done);
     p.ws.dec_desc = reinterpret_cast<pkv::DecodeDesc*>(w + L.dec_desc);

@@ -171,8 +171,11 @@ __device__ __noinline__ void merge_head1(const AttnParams& p, int u0, int n, int
 
 // Item descriptor as published in the item ring.
 enum : int { kItemDecode = 0, kItemMerge = 1 };
+// u: the chunk of a decode item, the part of a merge item; a merge item's k0
+// holds the done count it waits for (the sequence's chunks of every run of
+// the plan so far, this one included).
 struct ItemMeta {
-  int s, k0, k1, t, nchunks, u, hg, u0, kind;  // u: the chunk of a decode item, the part of a merge item
+  int s, k0, k1, t, nchunks, u, hg, u0, kind;
 };
 
 template <int KV, int D, typename OutT>
@@ -214,17 +217,11 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
   }
   __syncthreads();
   grid_dep_wait();  // the plan kernel's lists are complete from here on
-  if (!plan_matches(p)) {  // the same answer in every thread
-    if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
-    return;
-  }
   if (warp > HP + 1) return;  // launched with (HP + 2) warps; nothing else to do
   const int HG = p.Hkv / HP;
   // a merge is cut into G parts of HP query heads (one per consumer warp),
   // so that the merges of the last sequences spread over many CTAs
   const int MS = p.G;
-  const int n_dec = p.ws.dec_off[p.B] * HG;          // decode items, then
-  const int n_items = n_dec + *p.ws.n_merge * HG * MS;  // merge items
 
   if (warp == HP) {
     // ======================= copy warp =======================
@@ -327,6 +324,16 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     // latency never stalls the copy stream.  When the consumers hand an item
     // slot back, a split chunk they finished is reported to the merge items
     // through the sequence's done counter.
+    // the plan's sizes (the other warps do not need them); a workspace
+    // planned for other shapes gives no work
+    const bool planned = plan_matches_warp(p);
+    int32_t sz = 0;
+    if (lane == 0) sz = p.ws.dec_off[p.B];
+    if (lane == 1) sz = *p.ws.n_merge;
+    const int dec_units = __shfl_sync(0xffffffffu, sz, 0), merges = __shfl_sync(0xffffffffu, sz, 1);
+    if (!planned && lane == 0) atomicOr(p.err, kErrPlan);
+    const int n_dec = planned ? dec_units * HG : 0;             // decode items, then
+    const int n_items = planned ? n_dec + merges * HG * MS : 0;  // merge items
     constexpr int GS = 16;  // stages whose block-table entries are loaded together
     constexpr int32_t kPast = INT32_MIN;
     const int tok = lane & 15, half = lane >> 4;
@@ -344,7 +351,8 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     };
     // Publishes item x (descriptor e) into the next item slot, or the end
     // marker when x >= n_items, once the consumers have handed the slot back.
-    auto publish = [&](int x, const DecodeDesc& e) -> bool {
+    // run: how many runs of the plan came before this one (merge items).
+    auto publish = [&](int x, const DecodeDesc& e, int run) -> bool {
       if (!mbar_wait(iempty0 + 8 * islot, iphase ^ 1, p.err)) return false;
       retire(islot);
       unsigned char* it = items + islot * itemB;
@@ -378,7 +386,10 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
         const int hg = rest % HG;
         const int sm = p.ws.merge_list[rest / HG];
         const int u0 = p.ws.dec_off[sm];
-        const ItemMeta mm{sm, 0, 0, p.cu_q[sm], p.ws.dec_off[sm + 1] - u0, part, hg, u0, kItemMerge};
+        const int nch = p.ws.dec_off[sm + 1] - u0;
+        // the counts wrap modulo 2^32 on both sides
+        const int need = static_cast<int>((static_cast<unsigned>(run) + 1u) * static_cast<unsigned>(nch));
+        const ItemMeta mm{sm, need, 0, p.cu_q[sm], nch, part, hg, u0, kItemMerge};
         if (lane == 0) {
           *mp = mm;
           mbar_arrive(ifull0 + 8 * islot);
@@ -407,13 +418,31 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     };
     bool ok = true;
     int w = blockIdx.x;
+    // The claims of this run are base .. base + n_items - 1 (base a multiple
+    // of n_items, found once from the first claim; lane 0 only)
+    unsigned long long base = ~0ull;
+    int run = 0;
+    auto find_base = [&](unsigned long long c) {
+      if (base == ~0ull) {
+        const unsigned long long n = static_cast<unsigned long long>(n_items);
+        run = static_cast<int>(c / n);
+        base = c - c % n;
+      }
+    };
     while (ok && w < n_items && !flags[0]) {
-      int claim = 0;
-      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.work, 1);  // the next item, read at the end
+      // the next item (read at the end of the iteration)
+      unsigned long long c = 0;
+      if (lane == 0) c = atomicAdd(p.ws.work, 1ull);
       DecodeDesc d{};
       const bool is_dec = w < n_dec;
-      if (is_dec) d = p.ws.dec_desc[w / HG];
-      ok = publish(w, d);
+      int item_run = 0;
+      if (is_dec) {
+        d = p.ws.dec_desc[w / HG];
+      } else {  // a merge item needs the run number
+        if (lane == 0) find_base(c);
+        item_run = __shfl_sync(0xffffffffu, run, 0);
+      }
+      ok = publish(w, d, item_run);
       if (ok && is_dec) {
         const int head_off = (w - (w / HG) * HG) * HP;
         const int32_t* bt_row = p.bt + (int64_t)d.s * p.bt_stride;
@@ -448,11 +477,16 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
           }
         }
       }
-      w = __shfl_sync(0xffffffffu, claim, 0);
+      int next = 0;
+      if (lane == 0) {
+        find_base(c);
+        next = static_cast<int>(gridDim.x + (c - base));
+      }
+      w = __shfl_sync(0xffffffffu, next, 0);
     }
     // ---- the end: the consumers' end marker, the copy warp's end record,
     // and the last item's split chunk reported once its slot comes back
-    if (ok && !flags[0]) ok = publish(n_items, DecodeDesc{});
+    if (ok && !flags[0]) ok = publish(n_items, DecodeDesc{}, 0);
     if (!put_record(-1, true, -1)) ok = false;
     if (ok && !flags[0]) {
       const int n_last = islot ? pub1 : pub0;  // the slot published before the end marker
@@ -482,9 +516,12 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       int ready = 1;
       if (lane == 0) {
         const int32_t* cnt = p.ws.done + m.s * HG + m.hg;
-        if (ld_acquire(cnt) < m.nchunks) {
+        // done counts run on (modulo 2^32): compare the difference
+        auto short_of = [&]() { return static_cast<int>(static_cast<unsigned>(ld_acquire(cnt)) -
+                                                        static_cast<unsigned>(m.k0)) < 0; };
+        if (short_of()) {
           const long long t0 = clock64();
-          while (ld_acquire(cnt) < m.nchunks) {
+          while (short_of()) {
             __nanosleep(200);
             if (clock64() - t0 > kWaitLimitCycles) {
               atomicOr(p.err, kErrWaitTimeout);
@@ -687,18 +724,10 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
 
 template <int KV, int D, typename OutT>
 __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(AttnParams p) {
+  // the kernel that follows (the next layer's append or run) may launch and
+  // set up on the SMs this grid leaves; it waits for this grid to complete
+  launch_dependents();
   decode_body<KV, D, OutT>(p);
-  // every warp of the CTA is done with the counters; the last CTA of the
-  // grid leaves them reset for the next run over the same plan (a run
-  // without a matching plan writes nothing; the test has one answer for
-  // the whole grid)
-  if (plan_matches(p) && last_cta_of_grid(p.ws.dec_exit)) {
-    for (int i = threadIdx.x; i < p.B * p.Hkv; i += blockDim.x) p.ws.done[i] = 0;
-    if (threadIdx.x == 0) {
-      *p.ws.work = 0;
-      *p.ws.dec_exit = 0;
-    }
-  }
 }
 
 // ---------------------------------------------------------------- launch

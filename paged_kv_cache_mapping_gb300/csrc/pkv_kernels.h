@@ -67,14 +67,17 @@ struct PrefillDesc {
 struct Workspace {
   int32_t* dec_off;      // [B+1] prefix sums of decode chunk units (unit u0 + c = chunk c)
   int32_t* pf_off;       // [B+1] prefix sums of prefill row tiles
-  int32_t* work;         // [1] next decode item to hand out
+  // Claim counters.  Every run of a plan claims exactly as many decode
+  // items (prefill units) as the plan lists, one claim per item processed,
+  // so at the start of the k-th run after the plan a counter holds k times
+  // that number: a claim c names item c mod n of run c / n, and no run has
+  // to reset anything when it ends.  The plan zeroes them.
+  unsigned long long* work;     // [1] decode item claims
+  unsigned long long* pf_work;  // [1] tensor-core prefill unit claims
   int32_t* n_merge;      // [1] sequences split into more than one chunk
-  int32_t* pf_work;      // [1] next tensor-core prefill unit to hand out
-  int32_t* dec_exit;     // [1] decode CTAs finished (the last one resets the decode counters)
-  int32_t* pf_exit;      // [1] tensor-core prefill CTAs finished (the last one resets pf_work)
   int32_t* sig;          // [kPlanSig] what the plan was made for (plan_signature)
   int32_t* merge_list;   // [B] those sequences
-  int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group)
+  int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group), summed over runs
   DecodeDesc* dec_desc;  // [B * max_chunks] decode work: full chunks first, then ragged tails
   PrefillDesc* pf_desc;  // [max prefill tiles] prefill tiles in order
   float* part_o;         // [B * max_chunks, Hq, D] chunk outputs (normalised)
@@ -140,30 +143,19 @@ __host__ __device__ inline void plan_signature(const AttnParams& p, int32_t (&si
   sig[11] = p.decode_max_g;
 }
 
-// Every thread of a run kernel may call this after its dependency wait (the
-// signature is written by the plan kernel and not changed by a run).
-__device__ __forceinline__ bool plan_matches(const AttnParams& p) {
-  int32_t want[kPlanSig];
-  plan_signature(p, want);
-  bool ok = true;
+// The check by a whole warp after its dependency wait (the signature is
+// written by the plan kernel and not changed by a run): lane i < kPlanSig
+// compares word i, so that a warp makes kPlanSig loads, not 32 times as
+// many (every CTA of a grid reads the same few words).
+__device__ __forceinline__ bool plan_matches_warp(const AttnParams& p) {
+  const int lane = threadIdx.x & 31;
+  int32_t sig[kPlanSig];
+  plan_signature(p, sig);
+  int32_t want = 0;
 #pragma unroll
-  for (int i = 0; i < kPlanSig; ++i) ok &= __ldcg(p.ws.sig + i) == want[i];
-  return ok;
-}
-
-// Called by every thread of a run kernel at its end: true in the last CTA
-// of the grid to get there, after all the others have finished with the
-// run's counters (each CTA fences its own accesses before it reports).
-__device__ __forceinline__ bool last_cta_of_grid(int32_t* exit_count) {
-  __shared__ int last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(exit_count, 1) == static_cast<int>(gridDim.x) - 1;
-    __threadfence();
-  }
-  __syncthreads();
-  return last != 0;
+  for (int i = 0; i < kPlanSig; ++i) want = lane == i ? sig[i] : want;
+  const bool ok = lane >= kPlanSig || __ldcg(p.ws.sig + lane) == want;
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Launchers.  out_kind: 0 = f32, 1 = bf16.  kv: 0 = f32, 1 = bf16, 2 = e4m3.

@@ -126,10 +126,10 @@ constexpr int kPlanSeqs = 512;
 // One block: per-sequence work counts and their prefix sums, the decode
 // work list (every full chunk first, then the ragged last chunks, so that
 // the small pieces come last), the list of split sequences, the prefill
-// tile list, the counters of the run kernels reset, and the plan's
-// signature.  Reads device lengths; no host round trip.  A plan serves any
-// number of runs (one per layer) over the same lengths: each run's kernels
-// leave their counters reset when they finish.
+// tile list, the claim and done counters of the runs zeroed, and the
+// plan's signature.  Reads device lengths; no host round trip.  A plan
+// serves any number of runs (one per layer) over the same lengths: the
+// counters run on from one run to the next (see Workspace).
 __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   launch_dependents();  // the next kernel may start its set-up now
   // launched with programmatic dependent launch: the lengths may come from
@@ -190,10 +190,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   if (tid == 0) {
     p.ws.dec_off[B] = tot[0];
     p.ws.pf_off[B] = tot[3];
-    *p.ws.work = 0;
-    *p.ws.pf_work = 0;
-    *p.ws.dec_exit = 0;
-    *p.ws.pf_exit = 0;
+    *p.ws.work = 0ull;
+    *p.ws.pf_work = 0ull;
     *p.ws.n_merge = tot[4];
   }
   if (tid < kPlanSig) {

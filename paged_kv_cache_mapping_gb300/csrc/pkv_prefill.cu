@@ -61,7 +61,7 @@ template <int KV, int D, typename OutT>
 __global__ void __launch_bounds__(PrefillCfg<KV, D>::kThreads, 2) prefill_kernel(AttnParams p) {
   using C = PrefillCfg<KV, D>;
   using R = Ring<C::kRowB, C::kRowS, C::kST, C::kNS>;
-  if (!plan_matches(p)) {  // the same answer in every thread
+  if (!plan_matches_warp(p)) {  // the same answer in every thread
     if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
     return;
   }

@@ -93,10 +93,13 @@ __host__ __device__ constexpr uint32_t umma_idesc(int n, int b_mn) {
          ((uint32_t)(kTcRows >> 4) << 24);
 }
 
+// The MMA and commit wrappers are executed by the whole (converged) warp
+// and issue from one lane chosen by elect.sync: the operands are then the
+// same in every lane and stay in the uniform datapath.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
@@ -105,13 +108,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
 __device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                              uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -361,8 +367,10 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
           tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full);
       }
       if (!stream_kv(e, hk, g, false)) { *abort_flag = 1; break; }
+      // claim c of the plan's runs names unit c mod n_units (see Workspace)
       int claim = 0;
-      if (lane == 0) claim = gridDim.x + atomicAdd(p.ws.pf_work, 1);
+      if (lane == 0)
+        claim = static_cast<int>(gridDim.x + atomicAdd(p.ws.pf_work, 1ull) % static_cast<unsigned long long>(n_units));
       u = __shfl_sync(0xffffffffu, claim, 0);
     }
     if (aborted()) drain_copies(g, false);
@@ -408,7 +416,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         // this Q K^T (issue order is execution order)
         if (!mbar_wait_warp(k_full(st), ph, p.err)) return false;
         tc_fence_after();
-        if (lane == 0) {
+        {
           // a descriptor's start address is its low field (bytes >> 4): the
           // k steps add constant offsets to one base descriptor per operand
           const uint64_t dq = umma_desc(sQ, 16, 1024), dk = umma_desc(sK + st * Geo::kKVBytes, 16, 1024);
@@ -429,7 +437,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         const int gg = g + t;
         if (t + 1 < n_kt) {
           ok = issue_qk(gg + 1);
-        } else if (lane == 0) {
+        } else {
           umma_commit(q_empty);  // the unit's Q is no longer read
         }
         if (!ok) break;
@@ -438,7 +446,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
              (t > 0 || mbar_wait_warp(o_free, (q_it & 1) ^ 1, p.err));
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
+        {
           // P hi in columns 0-63 of the buffer, P lo in 64-127: 16 keys are
           // 8 columns; V is MN-major, 16 keys = 2048 bytes of each d half
           const uint32_t tp = tmem + pb * kTcKeys;
@@ -459,7 +467,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     if (!ok || aborted()) {
       // giving up: every MMA issued so far must finish before TMEM is freed
       *abort_flag = 1;
-      if (lane == 0) umma_commit(drain);
+      umma_commit(drain);
       __syncwarp();
       mbar_wait_warp(drain, 0, p.err);
     }
@@ -695,16 +703,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // kernel that follows launch and set up on the SMs this grid frees
   grid_dep_wait();
   launch_dependents();
-  const bool planned = plan_matches(p);  // one answer for the whole grid
-  if (planned)
+  if (plan_matches_warp(p))  // one answer for the whole grid
     prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v);
   else if (threadIdx.x == 0)
     atomicOr(p.err, kErrPlan);
-  // the last CTA leaves the unit counter reset for the next run of the plan
-  if (planned && last_cta_of_grid(p.ws.pf_exit) && threadIdx.x == 0) {
-    *p.ws.pf_work = 0;
-    *p.ws.pf_exit = 0;
-  }
 }
 
 // ---- host: tensor maps

@@ -102,6 +102,7 @@ def test_a_run_without_a_matching_plan_does_nothing_and_is_recorded():
     assert torch.isnan(o).all()
     # the mixed kernels check too: a decode plan run as a prefill batch
     m = DeviceStep(_mixed_tc())
+    expected = m.step().clone()  # the step's rows appended, then the full call
     ws = torch.empty(max(m.ws.numel(), a.ws.numel()), dtype=torch.uint8, device="cuda")
     pkv_attention_plan(a.q, a.cu_q, a.seq_lens, a.bt, a.caches[0][0], ws, max_q_len=1)
     o = torch.full_like(m.out, float("nan"))
@@ -113,7 +114,7 @@ def test_a_run_without_a_matching_plan_does_nothing_and_is_recorded():
     pkv_attention_run(m.q, m.cu_q, m.seq_lens, m.bt, *m.caches[0], m.wl.scale, o, ws, max_q_len=m.max_q_len)
     torch.cuda.synchronize()
     assert pkv_device_errors() == 0
-    assert torch.equal(o, m.step())
+    assert torch.equal(o, expected)
 
 
 def test_plan_and_layer_runs_replay_from_a_cuda_graph():
