@@ -543,6 +543,7 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
   p.window_left = window_left >= 0 ? window_left : -1;
   p.v_scale = kv == 2 ? v_scale : 1.0f;
   p.decode_max_g = 8;
+  p.kv_esize = esize(k_cache->dtype);
   if (kv == 0) {
     if (p.soft_cap > 0.f || p.window_left >= 0)
       return fail(PKV_ERR_UNSUPPORTED, "a soft cap or sliding window is built for bf16 and e4m3 caches");
@@ -558,6 +559,7 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
     p.ws.work = reinterpret_cast<unsigned long long*>(w + L.work);
     p.ws.pf_work = p.ws.work + 1;
     p.ws.n_merge = reinterpret_cast<int32_t*>(w + L.work + 16);
+    p.ws.pf_ctas = reinterpret_cast<int32_t*>(w + L.work + 20);
     p.ws.sig = reinterpret_cast<int32_t*>(w + L.work + 32);
     p.ws.merge_list = reinterpret_cast<int32_t*>(w + L.merge_list);
     p.ws.done = reinterpret_cast<int32_t*>(w + L.done);
@@ -576,7 +578,9 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
   p.pf_tq = c.tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
   p.path = !c.prefill ? 0 : (c.tc ? 2 : 1);
   // every argument is valid: the device's error word and SM count
-  return device_state(&p.err, &c.sms);
+  PKV_TRY(device_state(&p.err, &c.sms));
+  p.num_sms = c.sms;
+  return PKV_OK;
 }
 
 pkv_status launch_plan(const Call& c) {
@@ -606,10 +610,13 @@ pkv_status launch_run(const Call& c) {
   if (p.G <= p.decode_max_g) {
     const int64_t dec_seqs = std::min<int64_t>(p.B, p.T);
     // programmatic launch after the plan or the previous kernel of the
-    // stream, and after the tensor-core prefill (the decode kernel waits for
-    // its predecessor before reading anything); after the mma.sync prefill
-    // it is a plain launch
-    e = pkv::launch_decode(p, c.kv, c.out_kind, dec_seqs * pkv::max_chunks_for(c.max_ctx) * p.Hkv, c.sms, c.st,
+    // stream (the decode kernel waits for it before reading anything), and
+    // after the tensor-core prefill, beside which it runs (it waits for the
+    // prefill only before it exits); after the mma.sync prefill it is a
+    // plain launch
+    pkv::AttnParams pd = p;
+    pd.dec_concurrent = c.tc ? 1 : 0;
+    e = pkv::launch_decode(pd, c.kv, c.out_kind, dec_seqs * pkv::max_chunks_for(c.max_ctx) * p.Hkv, c.sms, c.st,
                            !c.prefill || c.tc);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }

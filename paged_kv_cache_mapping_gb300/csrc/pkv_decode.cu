@@ -216,7 +216,9 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     fence_barrier_init();
   }
   __syncthreads();
-  grid_dep_wait();  // the plan kernel's lists are complete from here on
+  // the plan kernel's lists are complete after this wait; beside the
+  // tensor-core prefill the wait is at the end (see decode_kernel)
+  if (!p.dec_concurrent) grid_dep_wait();
   if (warp > HP + 1) return;  // launched with (HP + 2) warps; nothing else to do
   const int HG = p.Hkv / HP;
   // a merge is cut into G parts of HP query heads (one per consumer warp),
@@ -328,8 +330,8 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     // planned for other shapes gives no work
     const bool planned = plan_matches_warp(p);
     int32_t sz = 0;
-    if (lane == 0) sz = p.ws.dec_off[p.B];
-    if (lane == 1) sz = *p.ws.n_merge;
+    if (lane == 0) sz = __ldcg(p.ws.dec_off + p.B);
+    if (lane == 1) sz = __ldcg(p.ws.n_merge);
     const int dec_units = __shfl_sync(0xffffffffu, sz, 0), merges = __shfl_sync(0xffffffffu, sz, 1);
     if (!planned && lane == 0) atomicOr(p.err, kErrPlan);
     const int n_dec = planned ? dec_units * HG : 0;             // decode items, then
@@ -384,12 +386,12 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       } else {
         const int part = (x - n_dec) % MS, rest = (x - n_dec) / MS;
         const int hg = rest % HG;
-        const int sm = p.ws.merge_list[rest / HG];
-        const int u0 = p.ws.dec_off[sm];
-        const int nch = p.ws.dec_off[sm + 1] - u0;
+        const int sm = __ldcg(p.ws.merge_list + rest / HG);
+        const int u0 = __ldcg(p.ws.dec_off + sm);
+        const int nch = __ldcg(p.ws.dec_off + sm + 1) - u0;
         // the counts wrap modulo 2^32 on both sides
         const int need = static_cast<int>((static_cast<unsigned>(run) + 1u) * static_cast<unsigned>(nch));
-        const ItemMeta mm{sm, need, 0, p.cu_q[sm], nch, part, hg, u0, kItemMerge};
+        const ItemMeta mm{sm, need, 0, __ldcg(p.cu_q + sm), nch, part, hg, u0, kItemMerge};
         if (lane == 0) {
           *mp = mm;
           mbar_arrive(ifull0 + 8 * islot);
@@ -418,17 +420,37 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     };
     bool ok = true;
     int w = blockIdx.x;
-    // The claims of this run are base .. base + n_items - 1 (base a multiple
-    // of n_items, found once from the first claim; lane 0 only)
+    // Claims.  Alone, a CTA's first item is its index and each item it
+    // processes claims the next: a run makes n_items claims, and claim c of
+    // the run's base .. base + n_items - 1 names item gridDim.x + c - base.
+    // Beside the prefill, CTAs start at different times (some only when a
+    // prefill CTA leaves its SM), so every item is claimed, the first one
+    // too: a run makes n_items + gridDim.x claims (each CTA one past the
+    // end), and claim c names item c - base.  base is a multiple of the run's
+    // claim count, found once from the first claim (lane 0 only).
+    const bool claim_all = p.dec_concurrent != 0;
+    const unsigned long long run_claims =
+        static_cast<unsigned long long>(n_items) + (claim_all ? gridDim.x : 0u);
     unsigned long long base = ~0ull;
     int run = 0;
     auto find_base = [&](unsigned long long c) {
       if (base == ~0ull) {
-        const unsigned long long n = static_cast<unsigned long long>(n_items);
-        run = static_cast<int>(c / n);
-        base = c - c % n;
+        run = static_cast<int>(c / run_claims);
+        base = c - c % run_claims;
       }
     };
+    if (claim_all) {
+      w = n_items;
+      if (n_items > 0) {
+        int first = 0;
+        if (lane == 0) {
+          const unsigned long long c = atomicAdd(p.ws.work, 1ull);
+          find_base(c);
+          first = static_cast<int>(c - base);
+        }
+        w = __shfl_sync(0xffffffffu, first, 0);
+      }
+    }
     while (ok && w < n_items && !flags[0]) {
       // the next item (read at the end of the iteration)
       unsigned long long c = 0;
@@ -437,7 +459,9 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       const bool is_dec = w < n_dec;
       int item_run = 0;
       if (is_dec) {
-        d = p.ws.dec_desc[w / HG];
+        const int4* dp = reinterpret_cast<const int4*>(p.ws.dec_desc + w / HG);
+        const int4 d0 = __ldcg(dp), d1 = __ldcg(dp + 1);
+        d = DecodeDesc{d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
       } else {  // a merge item needs the run number
         if (lane == 0) find_base(c);
         item_run = __shfl_sync(0xffffffffu, run, 0);
@@ -457,7 +481,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
             if (j < d.k1) {
               const int lb = p.bs_shift >= 0 ? (j >> p.bs_shift) : (j / p.bs);
               off[k] = j - lb * p.bs;
-              blk[k] = __ldg(bt_row + lb);
+              blk[k] = __ldcg(bt_row + lb);
             }
           }
           int32_t sl[GS / 2];
@@ -480,7 +504,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       int next = 0;
       if (lane == 0) {
         find_base(c);
-        next = static_cast<int>(gridDim.x + (c - base));
+        next = static_cast<int>((claim_all ? 0u : gridDim.x) + (c - base));
       }
       w = __shfl_sync(0xffffffffu, next, 0);
     }
@@ -728,6 +752,15 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
   // set up on the SMs this grid leaves; it waits for this grid to complete
   launch_dependents();
   decode_body<KV, D, OutT>(p);
+  // Beside the tensor-core prefill (dec_concurrent) this grid is launched as
+  // soon as every prefill CTA has passed its own dependency wait, which
+  // comes after the plan's kernel completed; so the plan's lists, and
+  // everything written before the plan, are in place when the decode CTAs
+  // start, and they read them through L2 (no stale L1 lines).  The prefill
+  // writes nothing the decode kernel reads.  Waiting for the prefill here,
+  // before the CTAs exit, makes this grid -- the last of the call --
+  // complete only after the prefill has.
+  if (p.dec_concurrent) grid_dep_wait();
 }
 
 // ---------------------------------------------------------------- launch

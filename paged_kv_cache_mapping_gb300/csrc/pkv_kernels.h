@@ -75,6 +75,7 @@ struct Workspace {
   unsigned long long* work;     // [1] decode item claims
   unsigned long long* pf_work;  // [1] tensor-core prefill unit claims
   int32_t* n_merge;      // [1] sequences split into more than one chunk
+  int32_t* pf_ctas;      // [1] CTAs the tensor-core prefill runs on beside the decode kernel
   int32_t* sig;          // [kPlanSig] what the plan was made for (plan_signature)
   int32_t* merge_list;   // [B] those sequences
   int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group), summed over runs
@@ -112,6 +113,9 @@ struct AttnParams {
   int32_t ns;            // decode: stages in the staging ring
   int32_t pf_tq;         // tensor-core prefill: query tokens per tile (0: the mma.sync prefill tiles)
   int32_t path;          // prefill kernel of the call: 0 none, 1 mma.sync, 2 tensor-core (tcgen05)
+  int32_t num_sms;       // SMs of the device (the plan splits them between prefill and decode)
+  int32_t kv_esize;      // bytes per cache element
+  int32_t dec_concurrent;  // decode kernel launched beside the tensor-core prefill (see decode_kernel)
   // variants: soft_cap > 0 turns a score s into soft_cap * tanh(s / soft_cap);
   // the kernels take x = cap_post * tanh(raw * cap_pre) in base 2, raw being
   // the q.k dot product of the stored values.  window_left >= 0: the query

@@ -123,6 +123,49 @@ __device__ __forceinline__ void write_pf_desc(const AttnParams& p, int s, const 
 // per chunk or tile); larger ones one thread per sequence.
 constexpr int kPlanSeqs = 512;
 
+// Key tiles (of the tensor-core prefill's 128 keys) that the prefill units
+// of sequence s cover, summed over its query tiles.
+__device__ __forceinline__ long long prefill_key_tiles(const AttnParams& p, const SeqCounts& c) {
+  long long n = 0;
+  for (int qt = 0; qt < c.pf; ++qt) {
+    const int r1 = c.q_s - qt * p.pf_tq, r0 = max(0, r1 - p.pf_tq);
+    const int kv_end = c.n - c.q_s + r1;
+    const int first = p.window_left >= 0 ? max(0, c.n - c.q_s + r0 - p.window_left) : 0;
+    n += (kv_end + 127) / 128 - first / 128;
+  }
+  return n;
+}
+
+// Measured rates on GB300 (sm_103a) that split the SMs of a call between the
+// tensor-core prefill and the decode kernel running beside it: a prefill
+// unit costs about kPfTileUs per 128-key tile (D = 128; half at D = 64)
+// plus kPfUnitUs of start and epilogue, a decode CTA streams about
+// kDecSmBytesPerUs of K/V, and all of them together at most kHbmBytesPerUs.
+constexpr float kPfTileUs = 1.3f;
+constexpr float kPfUnitUs = 3.5f;
+constexpr float kDecSmBytesPerUs = 45e3f;
+constexpr float kHbmBytesPerUs = 6.0e6f;
+
+// Prefill CTAs for a call with the given prefill key tiles (per KV head) and
+// decode bytes: the split that gives both kernels about the same time.
+__device__ inline int prefill_cta_split(const AttnParams& p, long long pf_tiles, int pf_units,
+                                        long long dec_bytes) {
+  const int S = p.num_sms;
+  if (dec_bytes == 0 || S < 2) return S;
+  const float pf = (float)pf_tiles * (float)p.Hkv * kPfTileUs * (p.D / 128.f) + (float)pf_units * kPfUnitUs;
+  const float hbm = (float)dec_bytes / kHbmBytesPerUs;
+  int best = 1;
+  float best_t = INFINITY;
+  for (int P = 1; P < S; ++P) {
+    const float t = fmaxf(pf / P, fmaxf((float)dec_bytes / ((S - P) * kDecSmBytesPerUs), hbm));
+    if (t < best_t) {
+      best_t = t;
+      best = P;
+    }
+  }
+  return best;
+}
+
 // One block: per-sequence work counts and their prefix sums, the decode
 // work list (every full chunk first, then the ragged last chunks, so that
 // the small pieces come last), the list of split sequences, the prefill
@@ -140,9 +183,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   const int B = p.B;
   const int per = (B + nth - 1) / nth;
   const int s0 = min(tid * per, B), s1 = min(s0 + per, B);
-  // First pass, counts and their prefix sums.
+  // First pass, counts and their prefix sums; with the tensor-core prefill,
+  // also the work that decides how the SMs are split between the kernels
+  __shared__ unsigned long long s_pf_tiles, s_dec_keys;
+  if (tid == 0) s_pf_tiles = s_dec_keys = 0ull;
+  __syncthreads();
   SeqCounts first{};  // the thread's first sequence, kept for the second pass
   int sum[5] = {0, 0, 0, 0, 0};
+  long long pf_tiles = 0, dec_keys = 0;
   for (int s = s0; s < s1; ++s) {
     const SeqCounts c = seq_counts(p, s, true);
     if (s == s0) first = c;
@@ -151,9 +199,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     sum[2] += c.tail;
     sum[3] += c.pf;
     sum[4] += c.dec > 1;
+    if (p.path == 2) {
+      pf_tiles += prefill_key_tiles(p, c);
+      if (c.dec > 0) dec_keys += c.n - decode_first_key(p, c.n);
+    }
+  }
+  if (p.path == 2) {
+    atomicAdd(&s_pf_tiles, (unsigned long long)pf_tiles);
+    atomicAdd(&s_dec_keys, (unsigned long long)dec_keys);
   }
   int off[5], tot[5];
-  block_scan<5>(sum, off, tot);
+  block_scan<5>(sum, off, tot);  // its barriers order the additions above
   __shared__ int4 sq_cnt[kPlanSeqs];  // dec, full, pf, n
   __shared__ int4 sq_off[kPlanSeqs];  // off[0..3]
   __shared__ int2 sq_len[kPlanSeqs];  // t0, q_s
@@ -193,6 +249,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
     *p.ws.work = 0ull;
     *p.ws.pf_work = 0ull;
     *p.ws.n_merge = tot[4];
+    *p.ws.pf_ctas = p.path == 2 ? prefill_cta_split(p, (long long)s_pf_tiles, tot[3] * p.Hkv,
+                                                    (long long)s_dec_keys * p.Hkv * p.D * p.kv_esize * 2)
+                                : p.num_sms;
   }
   if (tid < kPlanSig) {
     int32_t sig[kPlanSig];

@@ -205,7 +205,7 @@ __device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigne
 // and signals o_done[g % 2] when its P V has finished.
 template <int D, typename OutT>
 __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                                const CUtensorMap& tm_v) {
+                                                const CUtensorMap& tm_v, int active) {
   using Geo = TcGeom<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -370,7 +370,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       // claim c of the plan's runs names unit c mod n_units (see Workspace)
       int claim = 0;
       if (lane == 0)
-        claim = static_cast<int>(gridDim.x + atomicAdd(p.ws.pf_work, 1ull) % static_cast<unsigned long long>(n_units));
+        claim = static_cast<int>(active + atomicAdd(p.ws.pf_work, 1ull) % static_cast<unsigned long long>(n_units));
       u = __shfl_sync(0xffffffffu, claim, 0);
     }
     if (aborted()) drain_copies(g, false);
@@ -703,10 +703,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // kernel that follows launch and set up on the SMs this grid frees
   grid_dep_wait();
   launch_dependents();
-  if (plan_matches_warp(p))  // one answer for the whole grid
-    prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v);
-  else if (threadIdx.x == 0)
+  if (plan_matches_warp(p)) {  // one answer for the whole grid
+    // the plan gives the prefill part of the SMs (the decode kernel takes
+    // the rest): the CTAs past that many leave at once, and the others
+    // take the units (first unit = CTA index, then claims)
+    int32_t n = 0;
+    if ((threadIdx.x & 31) == 0) n = __ldcg(p.ws.pf_ctas);
+    const int active = min(static_cast<int>(gridDim.x), __shfl_sync(0xffffffffu, n, 0));
+    if (static_cast<int>(blockIdx.x) < active) prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v, active);
+  } else if (threadIdx.x == 0) {
     atomicOr(p.err, kErrPlan);
+  }
 }
 
 // ---- host: tensor maps
