@@ -72,10 +72,10 @@ struct TcGeom {
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   static constexpr int kOffX = kOffBar + 512;                 // row max / sum exchange [2][2][kTcRows]
   static constexpr int kSmem = kOffX + 4 * kTcRows * 4 + 1024; // + 1024-byte alignment slack
-  static constexpr uint32_t kTmemCols = 512;                  // S / P 2 x 128 columns, O D columns
-  static constexpr uint32_t kColO = 2 * kTcKeys;
+  static constexpr uint32_t kTmemCols = 512;                  // S / P 2 x 128 columns, O 2 x 128 columns
+  static constexpr uint32_t kColO = 2 * kTcKeys;              // O of unit parity b at kColO + 128 b
   static_assert(kSmem <= 227 * 1024, "shared memory");
-  static_assert(kColO + D <= kTmemCols, "tensor memory");
+  static_assert(kColO + 128 + D <= kTmemCols, "tensor memory");
 };
 
 // ---- tcgen05 / TMA wrappers
@@ -214,7 +214,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   const uint32_t sV = smem_u32(smem + Geo::kOffV);
   const uint32_t b0 = smem_u32(smem + Geo::kOffBar);
   auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
-  const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(22), drain = bar(23);
+  const uint32_t q_full = bar(0), q_empty = bar(1), drain = bar(23);
   auto k_full = [&](int s) { return bar(2 + s); };
   auto k_empty = [&](int s) { return bar(5 + s); };
   auto v_full = [&](int s) { return bar(8 + s); };
@@ -222,13 +222,16 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   auto s_full = [&](int b) { return bar(14 + b); };
   auto p_full = [&](int b) { return bar(18 + b); };
   auto o_done = [&](int b) { return bar(20 + b); };
+  auto o_free = [&](int b) { return bar(40 + b); };  // O buffer b read out by the epilogue
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 25);
-  // work units: the TMA warp claims them and passes each index to the MMA
-  // and softmax warps through a 2-slot ring
+  // work units: the TMA warp claims them and passes each index, with its
+  // descriptor, to the other warps through a 2-slot ring (no warp reads a
+  // descriptor from global memory on its way into a unit)
   auto unit_full = [&](int b) { return bar(26 + b); };
   auto unit_empty = [&](int b) { return bar(28 + b); };
   volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 30);
+  PrefillDesc* unit_desc = reinterpret_cast<PrefillDesc*>(smem + Geo::kOffBar + 384);  // [2]
   // the two softmax warps of TMEM lane quarter q trade per-row values
   // through buffer b of xval, paired by barrier xbar(q, b)
   auto xbar = [&](int q, int b) { return bar(32 + 2 * q + b); };
@@ -253,7 +256,8 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       mbar_init(p_full(b), 8);
       mbar_init(o_done(b), 1);
     }
-    mbar_init(o_free, 8);
+    mbar_init(o_free(0), 8);
+    mbar_init(o_free(1), 8);
     mbar_init(drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(unit_full(b), 1);
@@ -275,7 +279,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tO = tmem + Geo::kColO;  // S / P buffers: columns 0 .. 2 * kTcKeys - 1
+  const uint32_t tO = tmem + Geo::kColO;  // S / P buffers: columns 0 .. 2 * kTcKeys - 1; O buffers from here
 
   const int G = p.G, Hkv = p.Hkv;
   const int tq = p.pf_tq;  // query tokens per tile
@@ -290,8 +294,10 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys - kt0;
   };
   // K or V tiles of one unit, one TMA box (16 keys x one d half) per lane;
-  // the block-table entry of the next tile is loaded while this one is issued
-  auto stream_kv = [&](const PrefillDesc& e, int hk, int& g, bool is_v) -> bool {
+  // the block-table entry of the next tile is loaded while this one is
+  // issued.  claim: called (by the K producer) after the tile kt_claim is
+  // issued.
+  auto stream_kv = [&](const PrefillDesc& e, int hk, int& g, bool is_v, int kt_claim, auto&& claim) -> bool {
     const int64_t n_slots = p.num_blocks * p.bs;
     const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
     int kt0, n_kt;
@@ -326,6 +332,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       if (lane == 0) mbar_arrive_expect_tx(full, Geo::kKVBytes);
       __syncwarp();
       if (issuer) tma_load_3d(base + st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048, map, h * 64, hk, slot, full);
+      if (kt == kt_claim) claim();
       blk = nxt;
     }
     return true;
@@ -340,11 +347,13 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   if (warp == 0) {
     // ======================= TMA producer: units, Q and K =======================
     int g = 0, q_it = 0, ui = 0;
-    // hands unit index x (>= n_units: no more units) to the other warps
-    auto publish = [&](int x) -> bool {
+    // hands unit index x (>= n_units: no more units) and its descriptor to
+    // the other warps
+    auto publish = [&](int x, const PrefillDesc& e) -> bool {
       if (!mbar_wait_warp(unit_empty(ui & 1), ((ui >> 1) & 1) ^ 1, p.err)) return false;
       if (lane == 0) {
         unit_ring[ui & 1] = x;
+        unit_desc[ui & 1] = e;
         mbar_arrive(unit_full(ui & 1));
       }
       __syncwarp();
@@ -352,13 +361,24 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       return true;
     };
     // the first unit of a CTA is fixed; later ones are claimed in order, the
-    // longest first, once this warp has issued the current unit's last K tile
-    // (a few tiles ahead of the MMAs), so that CTAs finishing early take more
+    // longest first, when this warp has three K tiles of the current unit
+    // left to issue (its first tile, for shorter units): late enough that
+    // CTAs finishing early take more of the remaining units, early enough
+    // that the claim's round trip is over when the next unit's Q and K tiles
+    // are due
     int u = blockIdx.x;
     for (; !aborted(); ++q_it) {
-      if (!publish(u)) { *abort_flag = 1; break; }
+      PrefillDesc e{};
+      if (u < n_units) e = p.ws.pf_desc[u / Hkv];
+      if (!publish(u, e)) { *abort_flag = 1; break; }
       if (u >= n_units) break;
-      const PrefillDesc e = p.ws.pf_desc[u / Hkv];
+      // claim c of the plan's runs names unit c mod n_units (see Workspace)
+      unsigned long long c = 0;
+      auto claim = [&]() {
+        if (lane == 0) c = atomicAdd(p.ws.pf_work, 1ull);
+      };
+      int kt0, n_kt;
+      unit_tiles(e, kt0, n_kt);
       const int hk = u - (u / Hkv) * Hkv;
       if (!mbar_wait_warp(q_empty, (q_it & 1) ^ 1, p.err)) { *abort_flag = 1; break; }
       if (lane == 0) {
@@ -366,12 +386,10 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         for (int h = 0; h < Geo::kHalves; ++h)
           tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full);
       }
-      if (!stream_kv(e, hk, g, false)) { *abort_flag = 1; break; }
-      // claim c of the plan's runs names unit c mod n_units (see Workspace)
-      int claim = 0;
-      if (lane == 0)
-        claim = static_cast<int>(active + atomicAdd(p.ws.pf_work, 1ull) % static_cast<unsigned long long>(n_units));
-      u = __shfl_sync(0xffffffffu, claim, 0);
+      if (!stream_kv(e, hk, g, false, max(0, n_kt - 3), claim)) { *abort_flag = 1; break; }
+      int next = 0;
+      if (lane == 0) next = static_cast<int>(active + c % static_cast<unsigned long long>(n_units));
+      u = __shfl_sync(0xffffffffu, next, 0);
     }
     if (aborted()) drain_copies(g, false);
   } else if (warp == 2) {
@@ -381,12 +399,12 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     while (!aborted()) {
       if (!mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err)) { *abort_flag = 1; break; }
       const int u = unit_ring[ui & 1];
+      const PrefillDesc e = unit_desc[ui & 1];
       __syncwarp();
       if (lane == 0) mbar_arrive(unit_empty(ui & 1));
       ++ui;
       if (u >= n_units) break;
-      const PrefillDesc e = p.ws.pf_desc[u / Hkv];
-      if (!stream_kv(e, u - (u / Hkv) * Hkv, g, true)) { *abort_flag = 1; break; }
+      if (!stream_kv(e, u - (u / Hkv) * Hkv, g, true, -1, [] {})) { *abort_flag = 1; break; }
     }
     if (aborted()) drain_copies(g, true);
   } else if (warp == 1) {
@@ -397,17 +415,20 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     bool ok = true;
     for (; ok && !aborted(); ++q_it) {
       int u = n_units;
+      PrefillDesc e{};
       ok = mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err);
       if (ok) {
         u = unit_ring[ui & 1];
+        e = unit_desc[ui & 1];
         __syncwarp();
         if (lane == 0) mbar_arrive(unit_empty(ui & 1));
       }
       ++ui;
       if (!ok || u >= n_units) break;
-      const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       int kt0, n_kt;
       unit_tiles(e, kt0, n_kt);
+      const int ob = q_it & 1;  // O buffer of this unit (the epilogue may still read the other)
+      const uint32_t tOu = tO + ob * 128;
       ok = mbar_wait_warp(q_full, q_it & 1, p.err);
       // S[g % 2] = Q K^T for key tile g
       auto issue_qk = [&](int gg) -> bool {
@@ -443,7 +464,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         if (!ok) break;
         const int st = gg % kVStages, ph = (gg / kVStages) & 1, pb = gg & 1;
         ok = mbar_wait_warp(p_full(pb), (gg >> 1) & 1, p.err) && mbar_wait_warp(v_full(st), ph, p.err) &&
-             (t > 0 || mbar_wait_warp(o_free, (q_it & 1) ^ 1, p.err));
+             (t > 0 || mbar_wait_warp(o_free(ob), ((q_it >> 1) & 1) ^ 1, p.err));
         if (!ok) break;
         tc_fence_after();
         {
@@ -454,8 +475,8 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
           const uint32_t acc0 = t > 0;
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            umma_bf16_ta(tO, tp + kk * 8, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);                // P hi
-            umma_bf16_ta(tO, tp + kTcKeys / 2 + kk * 8, dv + kk * 128, kIdPV, 1);                  // P lo
+            umma_bf16_ta(tOu, tp + kk * 8, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);               // P hi
+            umma_bf16_ta(tOu, tp + kTcKeys / 2 + kk * 8, dv + kk * 128, kIdPV, 1);                 // P lo
           }
           umma_commit(o_done(pb));
           umma_commit(v_empty(st));
@@ -479,8 +500,58 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     constexpr int kHalfKeys = kTcKeys / 2;
     constexpr int kHalfD = D / 2;
-    int g = 0, ui = 0, xj = 0;
+    int g = 0, ui = 0, xj = 0, uc = 0;  // uc: units begun (O buffer parity)
     bool ok = true;
+    // The epilogue of a unit, run after the next unit's first tile (or at
+    // the end): wait for the unit's last P V, then write this thread's half
+    // of its row of O / l and hand the O buffer back.  The last P V's
+    // barrier cannot have moved on meanwhile: the next P V on that barrier
+    // needs a P that this warp writes only after the epilogue.
+    bool pend = false, pend_valid = false;
+    int pend_lg = 0, pend_ob = 0;
+    float pend_inv = 0.f;
+    OutT* pend_dst = nullptr;
+    auto epilogue = [&]() -> bool {
+      pend = false;
+      if (!mbar_wait_warp(o_done(pend_lg & 1), (pend_lg >> 1) & 1, p.err)) return false;
+      tc_fence_after();
+      const uint32_t to = tO + pend_ob * 128 + lane_off;
+      const float inv = pend_inv;
+#pragma unroll 1
+      for (int c = kHalfD * half; c < kHalfD * (half + 1); c += 32) {
+        uint32_t v[32];
+        tmem_ld32(to + c, v);
+        tmem_wait_ld();
+        if (pend_valid) {
+          OutT* d = pend_dst + c;
+          if ((reinterpret_cast<uintptr_t>(d) & 15u) == 0) {  // 16-byte stores (same rounding as store2)
+            constexpr int kPer = 16 / (int)sizeof(OutT);     // elements per store
+#pragma unroll
+            for (int j = 0; j < 32; j += kPer) {
+              uint4 w;
+              uint32_t* wu = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if constexpr (sizeof(OutT) == 2) {
+                  wu[e] = pack_bf16(__uint_as_float(v[j + 2 * e]) * inv, __uint_as_float(v[j + 2 * e + 1]) * inv);
+                } else {
+                  wu[e] = __float_as_uint(__uint_as_float(v[j + e]) * inv);
+                }
+              }
+              *reinterpret_cast<uint4*>(d + j) = w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              store2(d + j, __uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free(pend_ob));
+      return true;
+    };
     // gives this thread's value for its row to the partner thread and
     // returns the partner's (double-buffered; the partner makes the same
     // sequence of calls)
@@ -497,16 +568,20 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     };
     while (ok && !aborted()) {
       int u = n_units;
+      PrefillDesc e{};
       ok = mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err);
       if (ok) {
         u = unit_ring[ui & 1];
+        e = unit_desc[ui & 1];
         __syncwarp();
         if (lane == 0) mbar_arrive(unit_empty(ui & 1));
       }
       ++ui;
       if (!ok || u >= n_units) break;
-      const PrefillDesc e = p.ws.pf_desc[u / Hkv];
       const int hk = u - (u / Hkv) * Hkv;
+      const int ob = uc & 1;  // this unit's O buffer
+      const uint32_t tOu = tO + ob * 128;
+      ++uc;
       int kt0, n_kt;
       unit_tiles(e, kt0, n_kt);
       const int tok = r / G, hj = r - tok * G;
@@ -587,11 +662,11 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
 #pragma unroll 1
             for (int c = kHalfD * half; c < kHalfD * (half + 1); c += 32) {
               uint32_t v[32];
-              tmem_ld32(tO + lane_off + c, v);
+              tmem_ld32(tOu + lane_off + c, v);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-              tmem_st32(tO + lane_off + c, v);
+              tmem_st32(tOu + lane_off + c, v);
             }
             tmem_wait_st();
           }
@@ -635,53 +710,24 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(sb));
+        if (t == 0 && pend && !epilogue()) { ok = false; break; }  // the previous unit's
       }
       if (!ok) break;
-      // epilogue: O / l for valid rows, after the unit's last P V; the
-      // partners add their halves' sums and each writes half of the row
-      const int lg = g + n_kt - 1;
-      if (!mbar_wait_warp(o_done(lg & 1), (lg >> 1) & 1, p.err)) { ok = false; break; }
-      tc_fence_after();
+      // the row's sum: the partners add their halves; the epilogue (O / l)
+      // follows the next unit's first tile, so that its TMEM loads and
+      // global stores overlap that tile's MMAs
       float l_other;
       if (!trade(l, l_other)) { ok = false; break; }
       const float lt = l + l_other;
-      const float inv = valid && lt > 0.f ? p.v_scale / lt : 0.f;
-      OutT* dst = static_cast<OutT*>(p.out) + (int64_t)(e.t0 + i) * p.o_st + (int64_t)(hk * G + hj) * p.o_sh;
-#pragma unroll 1
-      for (int c = kHalfD * half; c < kHalfD * (half + 1); c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tO + lane_off + c, v);
-        tmem_wait_ld();
-        if (valid) {
-          OutT* d = dst + c;
-          if ((reinterpret_cast<uintptr_t>(d) & 15u) == 0) {  // 16-byte stores (same rounding as store2)
-            constexpr int kPer = 16 / (int)sizeof(OutT);     // elements per store
-#pragma unroll
-            for (int j = 0; j < 32; j += kPer) {
-              uint4 w;
-              uint32_t* wu = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                if constexpr (sizeof(OutT) == 2) {
-                  wu[e] = pack_bf16(__uint_as_float(v[j + 2 * e]) * inv, __uint_as_float(v[j + 2 * e + 1]) * inv);
-                } else {
-                  wu[e] = __float_as_uint(__uint_as_float(v[j + e]) * inv);
-                }
-              }
-              *reinterpret_cast<uint4*>(d + j) = w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2)
-              store2(d + j, __uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+      pend = true;
+      pend_lg = g + n_kt - 1;
+      pend_ob = ob;
+      pend_valid = valid;
+      pend_inv = valid && lt > 0.f ? p.v_scale / lt : 0.f;
+      pend_dst = static_cast<OutT*>(p.out) + (int64_t)(e.t0 + i) * p.o_st + (int64_t)(hk * G + hj) * p.o_sh;
       g += n_kt;
     }
+    if (ok && pend && !epilogue()) ok = false;  // the last unit's
     if (!ok) *abort_flag = 1;
   }
   // ---- teardown: every MMA of this CTA has completed (its results were
