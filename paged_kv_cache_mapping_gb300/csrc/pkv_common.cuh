@@ -27,21 +27,23 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 
 // Logical tiling.  Every tile and split boundary is a logical token position
 // so that the result does not depend on block_size or page placement.
-constexpr int kChunkBase = 128;       // smallest split-KV chunk (tokens)
+constexpr int kChunkBaseShift = 7;    // smallest split-KV chunk: 128 tokens ...
+constexpr int kChunkBaseShiftFp8 = 8; // ... 256 with an e4m3 cache (the same bytes per chunk)
 constexpr int kMaxChunks = 128;       // a sequence is split into at most this many chunks
 constexpr int kPrefillRows = 64;      // (query token, head) rows per prefill tile
 
-// Chunk length of a decoding sequence of n keys: the smallest 128 * 2^k
+// Chunk length of a decoding sequence of n keys: the smallest 2^base * 2^k
 // that splits it into at most kMaxChunks chunks, as a shift (chunk =
-// 1 << shift).  Depends on n only.
-__host__ __device__ inline int chunk_shift(int n) {
-  int k = 7;  // 128 tokens
+// 1 << shift).  Depends on n (and the cache format) only.
+__host__ __device__ inline int chunk_shift(int n, int base = kChunkBaseShift) {
+  int k = base;
   while ((((unsigned)n + (1u << k) - 1u) >> k) > (unsigned)kMaxChunks) ++k;
   return k;
 }
-__host__ __device__ inline int chunk_tokens(int n) { return 1 << chunk_shift(n); }
+__host__ __device__ inline int chunk_tokens(int n, int base = kChunkBaseShift) { return 1 << chunk_shift(n, base); }
 
-// Chunks of the longest sequence a block table of max_ctx tokens can hold.
+// Chunks of the longest sequence a block table of max_ctx tokens can hold
+// (with the smallest base: a bound for every format).
 __host__ __device__ inline int max_chunks_for(int64_t max_ctx) {
   if (max_ctx <= 0) return 1;
   const int n = max_ctx > 0x7fffffff ? 0x7fffffff : static_cast<int>(max_ctx);

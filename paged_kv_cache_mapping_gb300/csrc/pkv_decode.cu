@@ -10,8 +10,9 @@
 //
 // Design (GB300):
 //   * A work item is (sequence, logical chunk, group of HP KV heads).  The
-//     chunk length depends only on N_s (128 * 2^k tokens, at most 128
-//     chunks), so results depend neither on the batch nor on the page layout
+//     chunk length depends only on N_s (128 * 2^k tokens, 256 * 2^k with an
+//     e4m3 cache, at most 128 chunks), so results depend neither on the
+//     batch nor on the page layout
 //     ("How Easy Is It to Start Serving LLMs?", "3. Load balancing": long
 //     requests are split into chunks and a merge step stitches them).  The
 //     plan kernel lists the chunks once per call, every full chunk before

@@ -3,7 +3,8 @@
 // prefill kernels, built from the device lengths with no host round trip.
 //
 // Decode rows are cut into chunks whose length depends only on the
-// sequence's visible key count (128 * 2^k tokens, at most 128 chunks), so
+// sequence's visible key count (128 * 2^k tokens, 256 * 2^k with an e4m3
+// cache, at most 128 chunks), so
 // results depend neither on the batch nor on the page layout ("How Easy Is
 // It to Start Serving LLMs?", "3. Load balancing": long requests are split
 // into chunks and a merge step stitches them).  Prefill rows are cut into
@@ -55,6 +56,13 @@ __device__ __forceinline__ void block_scan(const int (&v)[K], int (&off)[K], int
   }
 }
 
+// Smallest decode chunk (as a shift): a chunk of an e4m3 cache holds twice
+// the tokens, so that its bytes, and the work an item carries against its
+// fixed costs (descriptor, query rows, partial result), stay the same.
+__device__ __forceinline__ int decode_chunk_base(const AttnParams& p) {
+  return p.kv_esize == 1 ? kChunkBaseShiftFp8 : kChunkBaseShift;
+}
+
 // First key a decoding query (position n - 1) sees.
 __device__ __forceinline__ int decode_first_key(const AttnParams& p, int n) {
   return p.window_left >= 0 && n - 1 - p.window_left > 0 ? n - 1 - p.window_left : 0;
@@ -81,7 +89,7 @@ __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool
   if (q_s == 1 && p.G <= p.decode_max_g) {
     // the visible keys [lo, n) are cut into chunks of 2^k from lo
     const int lo = decode_first_key(p, n);
-    const int k = chunk_shift(n - lo);
+    const int k = chunk_shift(n - lo, decode_chunk_base(p));
     c.dec = (int)(((unsigned)(n - lo) + (1u << k) - 1u) >> k);
     c.full = (n - lo) >> k;
     c.tail = c.dec - c.full;
@@ -99,7 +107,7 @@ __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool
 __device__ __forceinline__ void write_dec_desc(const AttnParams& p, int s, const SeqCounts& c, int off0, int off1,
                                                int off2, int tot_full, int ch) {
   const int first = decode_first_key(p, c.n);
-  const int k = chunk_shift(c.n - first);
+  const int k = chunk_shift(c.n - first, decode_chunk_base(p));
   const int k0 = first + (ch << k);
   int4* dst = reinterpret_cast<int4*>(p.ws.dec_desc + (ch < c.full ? off1 + ch : tot_full + off2));
   dst[0] = make_int4(s, k0, min(k0 + (1 << k), c.n), c.t0);
@@ -147,20 +155,30 @@ constexpr float kDecSmBytesPerUs = 45e3f;
 constexpr float kHbmBytesPerUs = 6.0e6f;
 
 // Prefill CTAs for a call with the given prefill key tiles (per KV head) and
-// decode bytes: the split that gives both kernels about the same time.
+// decode bytes: the split that gives the two kernels the shortest common
+// time.  Called by a whole warp; lane l tries l + 1, l + 33, ..
 __device__ inline int prefill_cta_split(const AttnParams& p, long long pf_tiles, int pf_units,
                                         long long dec_bytes) {
-  const int S = p.num_sms;
+  const int S = p.num_sms, lane = threadIdx.x & 31;
   if (dec_bytes == 0 || S < 2) return S;
   const float pf = (float)pf_tiles * (float)p.Hkv * kPfTileUs * (p.D / 128.f) + (float)pf_units * kPfUnitUs;
-  const float hbm = (float)dec_bytes / kHbmBytesPerUs;
-  int best = 1;
+  const float dec = (float)dec_bytes / kDecSmBytesPerUs, hbm = (float)dec_bytes / kHbmBytesPerUs;
+  int best = S;
   float best_t = INFINITY;
-  for (int P = 1; P < S; ++P) {
-    const float t = fmaxf(pf / P, fmaxf((float)dec_bytes / ((S - P) * kDecSmBytesPerUs), hbm));
+  for (int P = lane + 1; P < S; P += 32) {
+    const float t = fmaxf(__fdividef(pf, (float)P), fmaxf(__fdividef(dec, (float)(S - P)), hbm));
     if (t < best_t) {
       best_t = t;
       best = P;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // the smallest time, the fewest CTAs on a tie
+    const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+    const int op = __shfl_xor_sync(0xffffffffu, best, o);
+    if (ot < best_t || (ot == best_t && op < best)) {
+      best_t = ot;
+      best = op;
     }
   }
   return best;
@@ -243,15 +261,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
       for (int qt = lane; qt < c.pf; qt += 32) write_pf_desc(p, s, c, of.w, qt);
     }
   }
-  if (tid == 0) {
-    p.ws.dec_off[B] = tot[0];
-    p.ws.pf_off[B] = tot[3];
-    *p.ws.work = 0ull;
-    *p.ws.pf_work = 0ull;
-    *p.ws.n_merge = tot[4];
-    *p.ws.pf_ctas = p.path == 2 ? prefill_cta_split(p, (long long)s_pf_tiles, tot[3] * p.Hkv,
-                                                    (long long)s_dec_keys * p.Hkv * p.D * p.kv_esize * 2)
-                                : p.num_sms;
+  if (warp == 0) {
+    const int pf_ctas = p.path == 2 ? prefill_cta_split(p, (long long)s_pf_tiles, tot[3] * p.Hkv,
+                                                        (long long)s_dec_keys * p.Hkv * p.D * p.kv_esize * 2)
+                                    : p.num_sms;
+    if (lane == 0) {
+      p.ws.dec_off[B] = tot[0];
+      p.ws.pf_off[B] = tot[3];
+      *p.ws.work = 0ull;
+      *p.ws.pf_work = 0ull;
+      *p.ws.n_merge = tot[4];
+      *p.ws.pf_ctas = pf_ctas;
+    }
   }
   if (tid < kPlanSig) {
     int32_t sig[kPlanSig];
