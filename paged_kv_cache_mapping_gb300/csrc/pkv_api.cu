@@ -226,7 +226,7 @@ int64_t max_prefill_tiles(int64_t B, int64_t T, int64_t G) {
 }
 
 struct WsLayout {
-  size_t dec_off, pf_off, work, merge_list, done, dec_desc, pf_desc, part_o, part_lse, total;
+  size_t dec_off, pf_off, work, merge_desc, done, dec_desc, pf_desc, part_o, part_lse, total;
 };
 
 static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_ctx) {
@@ -237,7 +237,7 @@ static WsLayout ws_layout(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t
   L.dec_off = n;  n += align_up(sizeof(int32_t) * (B + 1), 256);
   L.pf_off = n;   n += align_up(sizeof(int32_t) * (B + 1), 256);
   L.work = n;     n += 256;  // claim counters, merge count, plan signature
-  L.merge_list = n; n += align_up(sizeof(int32_t) * B, 256);
+  L.merge_desc = n; n += align_up(sizeof(MergeDesc) * B * Hq, 256);
   L.done = n;     n += align_up(sizeof(int32_t) * B * Hkv, 256);
   L.dec_desc = n; n += align_up(sizeof(DecodeDesc) * units, 256);
   L.pf_desc = n;  n += align_up(sizeof(PrefillDesc) * max_prefill_tiles(B, T, G), 256);
@@ -561,7 +561,7 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
     p.ws.n_merge = reinterpret_cast<int32_t*>(w + L.work + 16);
     p.ws.pf_ctas = reinterpret_cast<int32_t*>(w + L.work + 20);
     p.ws.sig = reinterpret_cast<int32_t*>(w + L.work + 32);
-    p.ws.merge_list = reinterpret_cast<int32_t*>(w + L.merge_list);
+    p.ws.merge_desc = reinterpret_cast<pkv::MergeDesc*>(w + L.merge_desc);
     p.ws.done = reinterpret_cast<int32_t*>(w + L.done);
     p.ws.dec_desc = reinterpret_cast<pkv::DecodeDesc*>(w + L.dec_desc);
     p.ws.pf_desc = reinterpret_cast<pkv::PrefillDesc*>(w + L.pf_desc);
@@ -577,6 +577,9 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
                                      "caches with block sizes a multiple of 16 (max_q_len > 1 here)");
   p.pf_tq = c.tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
   p.path = !c.prefill ? 0 : (c.tc ? 2 : 1);
+  // the decode kernel's KV heads per item: the plan cuts merge items by it
+  p.hp = G <= p.decode_max_g ? pkv::decode_heads_per_item(kv, D, Hkv, G) : 1;
+  if (p.hp < 1) return fail(PKV_ERR_UNSUPPORTED, "no decode kernel geometry for these heads");
   // every argument is valid: the device's error word and SM count
   PKV_TRY(device_state(&p.err, &c.sms));
   p.num_sms = c.sms;

@@ -29,7 +29,7 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 // so that the result does not depend on block_size or page placement.
 constexpr int kChunkBaseShift = 7;    // smallest split-KV chunk: 128 tokens ...
 constexpr int kChunkBaseShiftFp8 = 8; // ... 256 with an e4m3 cache (the same bytes per chunk)
-constexpr int kMaxChunks = 128;       // a sequence is split into at most this many chunks
+constexpr int kMaxChunks = 512;       // a sequence is split into at most this many chunks
 constexpr int kPrefillRows = 64;      // (query token, head) rows per prefill tile
 
 // Chunk length of a decoding sequence of n keys: the smallest 2^base * 2^k

@@ -84,14 +84,22 @@ __host__ __device__ inline int decode_half_bytes(int hp) {  // the K (or V) half
 }
 template <int KV, int D>
 __host__ __device__ inline int decode_stage_bytes(int hp) { return 2 * decode_half_bytes<KV, D>(hp); }
+// An item slot: the item's query rows (a decode item) or the exchange of the
+// partial merges (a merge item: per consumer warp M, L and D values), then
+// the item's descriptor.
+template <int KV, int D>
+__host__ __device__ inline int decode_item_data_bytes(int hp, int G) {
+  const int q = hp * G * DecodeGeom<KV, D>::kQRowB, ex = hp * (D + 4) * 4;
+  return align16(q > ex ? q : ex);
+}
 template <int KV, int D>
 __host__ __device__ inline int decode_item_bytes(int hp, int G) {
-  return align16(hp * G * DecodeGeom<KV, D>::kQRowB + 64);
+  return decode_item_data_bytes<KV, D>(hp, G) + 64;
 }
 template <int KV, int D>
 __host__ __device__ inline size_t decode_smem(int hp, int ns, int G) {
   return (size_t)ns * decode_stage_bytes<KV, D>(hp) + 2 * decode_item_bytes<KV, D>(hp, G) +
-         DecodeGeom<KV, D>::kRecs * sizeof(StageRec) + (2 * ns + 4 + 2 * DecodeGeom<KV, D>::kRecs) * 8 + 16;
+         DecodeGeom<KV, D>::kRecs * sizeof(StageRec) + (2 * ns + 6 + 2 * DecodeGeom<KV, D>::kRecs) * 8 + 16;
 }
 
 // Output column d of accumulator tile mt, half (0: row g, 1: row g + 8).
@@ -109,15 +117,104 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   return v;
 }
 
-// A warp merges the chunk results of query head hq of a split sequence:
-// lane c holds the weights of chunks c, c+32, ..; lane l accumulates output
-// elements 4l .. 4l+3.  The loads of sixteen chunks are issued together
-// before they are used.
-// o = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M), chunks in order.
+struct MergePart {
+  float M, L;
+  float4 acc;
+};
+
+// A warp merges the results of chunks c0 .. c1-1 of query head hq of a split
+// sequence (unit u0 + c holds chunk c): lane l accumulates output elements
+// 4l .. 4l+3.  Returns, in every lane, the range's reference max M (log2
+// units) and L = sum_c 2^(lse_c - M), and in lane l its part of
+// acc = sum_c 2^(lse_c - M) o_c, chunks in order.  The range is taken in
+// blocks of 128 chunks (one, up to 128 chunks per warp): lane k holds the
+// weights of chunks k, k + 32, .. of a block, and the loads of sixteen
+// chunks are issued together before they are used; a later block with a
+// larger max rescales what came before.
+template <int D>
+__device__ __forceinline__ MergePart merge_range(const AttnParams& p, int u0, int c0, int c1, int hq, int lane) {
+  constexpr int kQ = 4;   // chunks per lane in a block
+  constexpr int kB = 16;  // chunks per batch of loads
+  const float* lse = p.ws.part_lse + (int64_t)u0 * p.Hq + hq;
+  const bool act = lane * 4 < D;
+  const float4* base = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)u0 * p.Hq * D) +
+                       (int64_t)hq * (D / 4) + lane;
+  const int64_t cstep = (int64_t)p.Hq * D / 4;  // float4s between chunks
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int b0 = c0; b0 < c1; b0 += 32 * kQ) {
+    const int n = min(c1 - b0, 32 * kQ);
+    float wv[kQ], lv[kQ];
+    float Mb = M;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+      const int c = lane + 32 * k;
+      lv[k] = c < n ? __ldcg(lse + (int64_t)(b0 + c) * p.Hq) : -INFINITY;
+      Mb = fmaxf(Mb, lv[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+    if (Mb != M) {  // the blocks before were weighted against the old max (none for the first)
+      const float a = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      L *= a;
+      acc.x *= a;
+      acc.y *= a;
+      acc.z *= a;
+      acc.w *= a;
+      M = Mb;
+    }
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+      wv[k] = lane + 32 * k < n ? exp2f(lv[k] - M) : 0.f;
+      l += wv[k];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    L += l;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+      if (32 * k >= n) break;
+#pragma unroll
+      for (int cb = 0; cb < 32; cb += kB) {
+        if (32 * k + cb >= n) break;
+        float4 v[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          const int c = 32 * k + cb + b;
+          v[b] = act && c < n ? __ldcg(base + (int64_t)(b0 + c) * cstep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          const float wc = __shfl_sync(0xffffffffu, wv[k], cb + b);  // 0 past n
+          acc.x += wc * v[b].x;
+          acc.y += wc * v[b].y;
+          acc.z += wc * v[b].z;
+          acc.w += wc * v[b].w;
+        }
+      }
+    }
+  }
+  return MergePart{M, L, acc};
+}
+
+// A warp merges all the chunk results of query head hq of a split sequence
+// of n <= 128 chunks and writes the output row (the merge items whose
+// heads each take one warp): lane c holds the weights of chunks c, c + 32,
+// ..; lane l accumulates output elements 4l .. 4l+3.  The first sixteen
+// chunks' loads go out with the log-sum-exp loads, the others sixteen at a
+// time.  o = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M), chunks in order.
 template <typename OutT, int D>
-__device__ __noinline__ void merge_head1(const AttnParams& p, int u0, int n, int hq, int t, int lane) {
-  constexpr int kQ = kMaxChunks / 32;  // chunks per lane
-  constexpr int kB = 16;               // chunks per batch of loads
+__device__ __noinline__ void merge_head(const AttnParams& p, int u0, int n, int hq, int t, int lane) {
+  constexpr int kQ = 4;   // chunks per lane
+  constexpr int kB = 16;  // chunks per batch of loads
+  const bool act = lane * 4 < D;
+  const float4* base = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)u0 * p.Hq * D) +
+                       (int64_t)hq * (D / 4) + lane;
+  const int64_t cstep = (int64_t)p.Hq * D / 4;  // float4s between chunks
+  float4 v[kB];
+#pragma unroll
+  for (int b = 0; b < kB; ++b) v[b] = act && b < n ? __ldcg(base + b * cstep) : make_float4(0.f, 0.f, 0.f, 0.f);
   float wv[kQ], lv[kQ];
   float M = -INFINITY;
 #pragma unroll
@@ -136,23 +233,19 @@ __device__ __noinline__ void merge_head1(const AttnParams& p, int u0, int n, int
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  const float inv_l = 1.f / L;
-  const bool act = lane * 4 < D;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* base = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)u0 * p.Hq * D) +
-                       (int64_t)hq * (D / 4) + lane;
-  const int64_t cstep = (int64_t)p.Hq * D / 4;  // float4s between chunks
 #pragma unroll
   for (int k = 0; k < kQ; ++k) {
     if (32 * k >= n) break;
 #pragma unroll
     for (int cb = 0; cb < 32; cb += kB) {
       if (32 * k + cb >= n) break;
-      float4 v[kB];
+      if (k + cb > 0) {
 #pragma unroll
-      for (int b = 0; b < kB; ++b) {
-        const int c = 32 * k + cb + b;
-        v[b] = act && c < n ? __ldcg(base + c * cstep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int b = 0; b < kB; ++b) {
+          const int c = 32 * k + cb + b;
+          v[b] = act && c < n ? __ldcg(base + c * cstep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
@@ -165,6 +258,17 @@ __device__ __noinline__ void merge_head1(const AttnParams& p, int u0, int n, int
     }
   }
   if (!act) return;
+  const float inv_l = 1.f / L;
+  OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)hq * p.o_sh + 4 * lane;
+  store2(dst, acc.x * inv_l, acc.y * inv_l);
+  store2(dst + 2, acc.z * inv_l, acc.w * inv_l);
+}
+
+// Stores lane l's elements 4l .. 4l+3 of query head hq of row t: acc / L.
+template <typename OutT, int D>
+__device__ __forceinline__ void store_merged(const AttnParams& p, int t, int hq, int lane, float L, float4 acc) {
+  if (lane * 4 >= D) return;
+  const float inv_l = 1.f / L;
   OutT* dst = static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)hq * p.o_sh + 4 * lane;
   store2(dst, acc.x * inv_l, acc.y * inv_l);
   store2(dst + 2, acc.z * inv_l, acc.w * inv_l);
@@ -172,12 +276,67 @@ __device__ __noinline__ void merge_head1(const AttnParams& p, int u0, int n, int
 
 // Item descriptor as published in the item ring.
 enum : int { kItemDecode = 0, kItemMerge = 1 };
-// u: the chunk of a decode item, the part of a merge item; a merge item's k0
-// holds the done count it waits for (the sequence's chunks of every run of
-// the plan so far, this one included).
+// u: the chunk of a decode item, the first query head (within the group) of
+// a merge item; a merge item's k0 holds the done count it waits for (the
+// sequence's chunks of every run of the plan so far, this one included) and
+// its k1 holds H | (R << 8) (see MergeDesc).
 struct ItemMeta {
   int s, k0, k1, t, nchunks, u, hg, u0, kind;
 };
+
+// Consumer warp h's part of merge item m: H query heads from m.u of the
+// group's HP * G, each merged by R warps over R ranges of the chunks
+// (H * R = HP); warp h takes head m.u + h / R and range h % R.  With R > 1
+// the partial merges of a head meet in the item slot's data area (warp h:
+// M, L, then its D values), exchanged through the slot's barrier mb (phase
+// mph), and the warp of range 0 combines them:
+// o = sum_r 2^(M_r - M*) acc_r / sum_r 2^(M_r - M*) L_r.  Out of line, so
+// that the decode loop's code stays as it is.  Returns false if the wait for
+// the other warps gave up.
+template <typename OutT, int D>
+__device__ __noinline__ bool merge_item(const AttnParams& p, int u0, int n, int hq0, int t, int k1, int h, int lane,
+                                        unsigned char* it, uint32_t mb, int mph, int ready) {
+  const int R = k1 >> 8;
+  const int r = h % R;
+  const int hq = hq0 + h / R;
+  MergePart mp{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (ready) mp = merge_range<D>(p, u0, r * n / R, (r + 1) * n / R, hq, lane);
+  if (R == 1) {
+    if (ready) store_merged<OutT, D>(p, t, hq, lane, mp.L, mp.acc);
+    return true;
+  }
+  float* ex = reinterpret_cast<float*>(it) + h * (D + 4);
+  if (lane == 0) {
+    ex[0] = mp.M;
+    ex[1] = mp.L;
+  }
+  if (lane * 4 < D) *reinterpret_cast<float4*>(ex + 4 + 4 * lane) = mp.acc;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(mb);
+  if (r != 0) return true;
+  if (!mbar_wait_warp(mb, mph, p.err)) return false;
+  if (!ready) return true;
+  const float* e0 = reinterpret_cast<const float*>(it) + h * (D + 4);
+  float Ms = -INFINITY;
+  for (int q = 0; q < R; ++q) Ms = fmaxf(Ms, e0[q * (D + 4)]);
+  float Ls = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q = 0; q < R; ++q) {
+    const float* e = e0 + q * (D + 4);
+    const float wq = exp2f(e[0] - Ms);
+    Ls += wq * e[1];
+    if (lane * 4 < D) {
+      const float4 v = *reinterpret_cast<const float4*>(e + 4 + 4 * lane);
+      a.x += wq * v.x;
+      a.y += wq * v.y;
+      a.z += wq * v.z;
+      a.w += wq * v.w;
+    }
+  }
+  store_merged<OutT, D>(p, t, hq, lane, Ls, a);
+  return true;
+}
+
 
 template <int KV, int D, typename OutT>
 __device__ __forceinline__ void decode_body(const AttnParams& p) {
@@ -198,7 +357,9 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NS;
   const uint32_t ifull0 = empty0 + 8 * NS, iempty0 = ifull0 + 16;
   const uint32_t rfull0 = iempty0 + 16, rempty0 = rfull0 + 8 * NR;
-  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * NS + 4 + 2 * NR);  // [0] abort
+  const uint32_t mex0 = rempty0 + 8 * NR;  // [2] partial merges of the item in slot i written
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * NS + 6 + 2 * NR);  // [0] abort
+  const int itemD = decode_item_data_bytes<KV, D>(HP, G);  // the descriptor's offset in a slot
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -213,6 +374,8 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       mbar_init(rfull0 + 8 * i, 32);
       mbar_init(rempty0 + 8 * i, 32);
     }
+    mbar_init(mex0, HP);
+    mbar_init(mex0 + 8, HP);
     flags[0] = 0;
     fence_barrier_init();
   }
@@ -222,9 +385,6 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
   if (!p.dec_concurrent) grid_dep_wait();
   if (warp > HP + 1) return;  // launched with (HP + 2) warps; nothing else to do
   const int HG = p.Hkv / HP;
-  // a merge is cut into G parts of HP query heads (one per consumer warp),
-  // so that the merges of the last sequences spread over many CTAs
-  const int MS = p.G;
 
   if (warp == HP) {
     // ======================= copy warp =======================
@@ -336,7 +496,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     const int dec_units = __shfl_sync(0xffffffffu, sz, 0), merges = __shfl_sync(0xffffffffu, sz, 1);
     if (!planned && lane == 0) atomicOr(p.err, kErrPlan);
     const int n_dec = planned ? dec_units * HG : 0;             // decode items, then
-    const int n_items = planned ? n_dec + merges * HG * MS : 0;  // merge items
+    const int n_items = planned ? n_dec + merges : 0;           // merge items
     constexpr int GS = 16;  // stages whose block-table entries are loaded together
     constexpr int32_t kPast = INT32_MIN;
     const int tok = lane & 15, half = lane >> 4;
@@ -360,7 +520,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       retire(islot);
       unsigned char* it = items + islot * itemB;
       const int q_rows = HP * G;
-      ItemMeta* mp = reinterpret_cast<ItemMeta*>(it + q_rows * QRowB);
+      ItemMeta* mp = reinterpret_cast<ItemMeta*>(it + itemD);
       if (x >= n_items) {
         if (lane == 0) {
           mp->s = -1;
@@ -385,14 +545,11 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
             bulk_g2s(smem_u32(it + r * QRowB), q0 + (int64_t)r * p.q_sh, QRowB, ifull0 + 8 * islot);
         }
       } else {
-        const int part = (x - n_dec) % MS, rest = (x - n_dec) / MS;
-        const int hg = rest % HG;
-        const int sm = __ldcg(p.ws.merge_list + rest / HG);
-        const int u0 = __ldcg(p.ws.dec_off + sm);
-        const int nch = __ldcg(p.ws.dec_off + sm + 1) - u0;
+        const int4* mdp = reinterpret_cast<const int4*>(p.ws.merge_desc + (x - n_dec));
+        const int4 md0 = __ldcg(mdp), md1 = __ldcg(mdp + 1);  // s, hg, h0, hr | nchunks, u0, t
         // the counts wrap modulo 2^32 on both sides
-        const int need = static_cast<int>((static_cast<unsigned>(run) + 1u) * static_cast<unsigned>(nch));
-        const ItemMeta mm{sm, need, 0, __ldcg(p.cu_q + sm), nch, part, hg, u0, kItemMerge};
+        const int need = static_cast<int>((static_cast<unsigned>(run) + 1u) * static_cast<unsigned>(md1.x));
+        const ItemMeta mm{md0.x, need, md0.w, md1.z, md1.x, md0.z, md0.y, md1.y, kItemMerge};
         if (lane == 0) {
           *mp = mm;
           mbar_arrive(ifull0 + 8 * islot);
@@ -526,13 +683,14 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
   const int h = warp;
   const int g4 = lane >> 2, t4 = lane & 3;  // fragment row / column-pair index
   int slot = 0, phase = 0, islot = 0, iphase = 0;
+  int mphase = 0;  // bit i: the phase of slot i's exchange barrier
   for (;;) {
     if (!mbar_wait(ifull0 + 8 * islot, iphase, p.err)) {
       flags[0] = 1;
       return;
     }
-    const unsigned char* it = items + islot * itemB;
-    const ItemMeta m = *reinterpret_cast<const ItemMeta*>(it + HP * G * QRowB);
+    unsigned char* it = items + islot * itemB;
+    const ItemMeta m = *reinterpret_cast<const ItemMeta*>(it + itemD);
     if (m.s < 0) return;  // no more items
     const int g = m.hg * HP + h;  // KV head of this warp
     const int hq0 = g * G;
@@ -558,11 +716,14 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       }
       ready = __shfl_sync(0xffffffffu, ready, 0);
       __syncwarp();
-      if (ready) {
-        // part m.u of the group's HP * G query heads: HP heads, warp h
-        // merges one of them
-        merge_head1<OutT, D>(p, m.u0, m.nchunks, m.hg * HP * G + m.u * HP + h, m.t, lane);
+      const int R = m.k1 >> 8;
+      if (R == 1 && m.nchunks <= 128) {  // one warp per head
+        if (ready) merge_head<OutT, D>(p, m.u0, m.nchunks, m.hg * HP * G + m.u + h, m.t, lane);
+      } else if (!merge_item<OutT, D>(p, m.u0, m.nchunks, m.hg * HP * G + m.u, m.t, m.k1, h, lane, it,
+                                      mex0 + 8 * islot, (mphase >> islot) & 1, ready)) {
+        flags[0] = 1;
       }
+      if (R > 1) mphase ^= 1 << islot;
       __syncwarp();
       if (lane == 0) mbar_arrive(iempty0 + 8 * islot);
       if (++islot == 2) {
@@ -781,8 +942,7 @@ static bool decode_geometry(int Hkv, int G, int& hp, int& ns) {
 template <int KV, int D, typename OutT>
 static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms, cudaStream_t st, bool pdl) {
   int hp = 1, ns = 3;
-  if (!decode_geometry<KV, D>(p.Hkv, p.G, hp, ns)) return cudaErrorInvalidConfiguration;
-  p.hp = hp;
+  if (!decode_geometry<KV, D>(p.Hkv, p.G, hp, ns) || hp != p.hp) return cudaErrorInvalidConfiguration;
   p.ns = ns;
   const size_t smem = decode_smem<KV, D>(hp, ns, p.G);
   auto kern = decode_kernel<KV, D, OutT>;
@@ -793,10 +953,20 @@ static cudaError_t launch_decode_t(AttnParams p, int64_t max_items, int num_sms,
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
   if (occ < 1) occ = 1;
   int64_t grid = (int64_t)num_sms * occ;
-  const int64_t items = (max_items + hp - 1) / hp + (int64_t)p.B * (p.Hkv / hp);  // chunks + merges
+  const int64_t items = (max_items + hp - 1) / hp + (int64_t)p.B * p.Hq;  // chunks + merges
   if (grid > items) grid = items;
   if (grid < 1) return cudaSuccess;
   return launch_ex(kern, dim3((unsigned)grid), dim3(threads), smem, st, pdl, p);
+}
+
+int decode_heads_per_item(int kv, int D, int Hkv, int G) {
+  int hp = 0, ns = 0;
+  bool ok;
+  if (kv == 1)
+    ok = D == 128 ? decode_geometry<1, 128>(Hkv, G, hp, ns) : decode_geometry<1, 64>(Hkv, G, hp, ns);
+  else
+    ok = D == 128 ? decode_geometry<2, 128>(Hkv, G, hp, ns) : decode_geometry<2, 64>(Hkv, G, hp, ns);
+  return ok ? hp : 0;
 }
 
 cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,

@@ -54,6 +54,21 @@ struct DecodeDesc {
   int32_t pad;
 };
 
+// One merge item: H query heads (h0 .. h0+H-1 of head group hg's HP * G) of a
+// split sequence, each merged by R consumer warps over R ranges of its
+// nchunks chunks (H * R = HP), the R partial merges then combined in shared
+// memory.
+struct MergeDesc {
+  int32_t s;        // sequence
+  int32_t hg;       // head group
+  int32_t h0;       // first query head of the item within the group
+  int32_t hr;       // H | (R << 8)
+  int32_t nchunks;  // chunks of the sequence
+  int32_t u0;       // unit of its first chunk
+  int32_t t;        // packed row of its query token
+  int32_t pad;
+};
+
 // One prefill tile: 64 consecutive (token, head-of-group) rows of a sequence.
 struct PrefillDesc {
   int32_t s;
@@ -74,10 +89,10 @@ struct Workspace {
   // to reset anything when it ends.  The plan zeroes them.
   unsigned long long* work;     // [1] decode item claims
   unsigned long long* pf_work;  // [1] tensor-core prefill unit claims
-  int32_t* n_merge;      // [1] sequences split into more than one chunk
+  int32_t* n_merge;      // [1] merge items
   int32_t* pf_ctas;      // [1] CTAs the tensor-core prefill runs on beside the decode kernel
   int32_t* sig;          // [kPlanSig] what the plan was made for (plan_signature)
-  int32_t* merge_list;   // [B] those sequences
+  MergeDesc* merge_desc;  // [B * Hq] merge items, in sequence order
   int32_t* done;         // [B * Hkv] finished chunks per (sequence, head group), summed over runs
   DecodeDesc* dec_desc;  // [B * max_chunks] decode work: full chunks first, then ragged tails
   PrefillDesc* pf_desc;  // [max prefill tiles] prefill tiles in order
@@ -130,7 +145,7 @@ struct AttnParams {
 // the workspace and checked by every kernel of a run before it reads the
 // plan's lists: a run whose call disagrees with the plan in the workspace
 // does no work and records kErrPlan.
-constexpr int kPlanSig = 12;
+constexpr int kPlanSig = 13;
 constexpr int32_t kPlanMagic = 0x504b5631;  // "PKV1"
 __host__ __device__ inline void plan_signature(const AttnParams& p, int32_t (&sig)[kPlanSig]) {
   sig[0] = kPlanMagic;
@@ -145,6 +160,7 @@ __host__ __device__ inline void plan_signature(const AttnParams& p, int32_t (&si
   sig[9] = p.path;
   sig[10] = p.window_left;
   sig[11] = p.decode_max_g;
+  sig[12] = p.hp;
 }
 
 // The check by a whole warp after its dependency wait (the signature is
@@ -190,6 +206,9 @@ inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 cudaError_t set_smem_attr(const void* kernel, size_t bytes);
 
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t st);
+// KV heads per decode item (the decode kernel's consumer warps) for a
+// cache format and head shape; 0 if the decode kernel cannot be built for it.
+int decode_heads_per_item(int kv, int D, int Hkv, int G);
 cudaError_t launch_decode(const AttnParams& p, int kv, int out_kind, int64_t max_items, int num_sms,
                           cudaStream_t st, bool pdl);
 

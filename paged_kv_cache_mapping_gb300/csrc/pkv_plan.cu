@@ -73,14 +73,34 @@ __device__ __forceinline__ int decode_first_key(const AttnParams& p, int n) {
 struct SeqCounts {
   int dec, full, tail, pf;  // decode chunks (all, full, ragged last), prefill tiles
   int n, t0, q_s;           // the lengths they came from
+  int cls;                  // size class of the decode chunks (0: the smallest chunk)
+  int mi;                   // merge items (split sequences)
 };
+
+// How the merge of a sequence of n chunks is cut: R consumer warps (a
+// divisor of HP) share each query head, each merging at most 64 chunks where
+// it can, so an item carries H = HP / R heads.  Depends on n and HP only.
+__device__ __forceinline__ void merge_split(int n, int hp, int& H, int& R) {
+  R = hp;
+  for (int r = 1; r <= hp; ++r) {
+    if (hp % r == 0 && 64 * r >= n) {
+      R = r;
+      break;
+    }
+  }
+  H = hp / R;
+}
+
+// The full chunks of the decode list are ordered by size, the largest first
+// (sequences of one size in order), so that the longest items start first.
+constexpr int kChunkClasses = 16;
 
 __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool record) {
   // L2 loads: the lengths may have been written by the previous kernel
   const int c0 = __ldcg(p.cu_q + s), c1 = __ldcg(p.cu_q + s + 1);
   const int q_s = c1 - c0;
   const int n = __ldcg(p.seq_lens + s);
-  SeqCounts c{0, 0, 0, 0, n, c0, q_s};
+  SeqCounts c{0, 0, 0, 0, n, c0, q_s, 0, 0};
   if (q_s == 0) return c;
   if (q_s < 0 || q_s > n || (int64_t)n > (int64_t)p.max_blocks * p.bs || c0 < 0 || c1 > p.T) {
     if (record) atomicOr(p.err, kErrLengths);
@@ -93,6 +113,12 @@ __device__ __forceinline__ SeqCounts seq_counts(const AttnParams& p, int s, bool
     c.dec = (int)(((unsigned)(n - lo) + (1u << k) - 1u) >> k);
     c.full = (n - lo) >> k;
     c.tail = c.dec - c.full;
+    c.cls = min(k - decode_chunk_base(p), kChunkClasses - 1);
+    if (c.dec > 1) {
+      int H, R;
+      merge_split(c.dec, p.hp, H, R);
+      c.mi = (p.Hkv / p.hp) * R * p.G;
+    }
   } else {
     c.pf = p.pf_tq > 0 ? (q_s + p.pf_tq - 1) / p.pf_tq
                        : (int)(((int64_t)q_s * p.G + kPrefillRows - 1) / kPrefillRows);
@@ -112,6 +138,18 @@ __device__ __forceinline__ void write_dec_desc(const AttnParams& p, int s, const
   int4* dst = reinterpret_cast<int4*>(p.ws.dec_desc + (ch < c.full ? off1 + ch : tot_full + off2));
   dst[0] = make_int4(s, k0, min(k0 + (1 << k), c.n), c.t0);
   dst[1] = make_int4(c.dec, off0, ch, 0);
+}
+
+// Descriptor of merge item k of split sequence s (its items start at off4):
+// head group k / (R G), heads (k mod R G) * H .. + H - 1 of the group.
+__device__ __forceinline__ void write_merge_desc(const AttnParams& p, int s, const SeqCounts& c, int off0, int off4,
+                                                 int k) {
+  int H, R;
+  merge_split(c.dec, p.hp, H, R);
+  const int per = R * p.G;
+  int4* dst = reinterpret_cast<int4*>(p.ws.merge_desc + off4 + k);
+  dst[0] = make_int4(s, k / per, (k % per) * H, H | (R << 8));
+  dst[1] = make_int4(c.dec, off0, c.t0, 0);
 }
 
 // Descriptor of prefill tile qt of sequence s (its tiles start at off3).
@@ -185,8 +223,8 @@ __device__ inline int prefill_cta_split(const AttnParams& p, long long pf_tiles,
 }
 
 // One block: per-sequence work counts and their prefix sums, the decode
-// work list (every full chunk first, then the ragged last chunks, so that
-// the small pieces come last), the list of split sequences, the prefill
+// work list (every full chunk first, the largest chunks first, then the
+// ragged last chunks, so that the small pieces come last), the list of split sequences, the prefill
 // tile list, the claim and done counters of the runs zeroed, and the
 // plan's signature.  Reads device lengths; no host round trip.  A plan
 // serves any number of runs (one per layer) over the same lengths: the
@@ -208,15 +246,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   __syncthreads();
   SeqCounts first{};  // the thread's first sequence, kept for the second pass
   int sum[5] = {0, 0, 0, 0, 0};
+  int cls[kChunkClasses];  // full chunks per size class
+#pragma unroll
+  for (int j = 0; j < kChunkClasses; ++j) cls[j] = 0;
   long long pf_tiles = 0, dec_keys = 0;
   for (int s = s0; s < s1; ++s) {
     const SeqCounts c = seq_counts(p, s, true);
     if (s == s0) first = c;
+#pragma unroll
+    for (int j = 0; j < kChunkClasses; ++j) cls[j] += j == c.cls ? c.full : 0;
     sum[0] += c.dec;
     sum[1] += c.full;
     sum[2] += c.tail;
     sum[3] += c.pf;
-    sum[4] += c.dec > 1;
+    sum[4] += c.mi;
     if (p.path == 2) {
       pf_tiles += prefill_key_tiles(p, c);
       if (c.dec > 0) dec_keys += c.n - decode_first_key(p, c.n);
@@ -228,37 +271,57 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   }
   int off[5], tot[5];
   block_scan<5>(sum, off, tot);  // its barriers order the additions above
+  // full chunks: class j starts after every larger class
+  int cls_off[kChunkClasses], cls_tot[kChunkClasses];
+  block_scan<kChunkClasses>(cls, cls_off, cls_tot);
+  {
+    int base = 0;
+#pragma unroll
+    for (int j = kChunkClasses - 1; j >= 0; --j) {
+      cls_off[j] += base;
+      base += cls_tot[j];
+    }
+  }
   __shared__ int4 sq_cnt[kPlanSeqs];  // dec, full, pf, n
   __shared__ int4 sq_off[kPlanSeqs];  // off[0..3]
-  __shared__ int2 sq_len[kPlanSeqs];  // t0, q_s
+  __shared__ int4 sq_len[kPlanSeqs];  // t0, q_s, mi, off[4]
   const bool by_warp = B <= kPlanSeqs;
   for (int s = s0; s < s1; ++s) {
     const SeqCounts c = s == s0 ? first : seq_counts(p, s, false);
     p.ws.dec_off[s] = off[0];
     p.ws.pf_off[s] = off[3];
-    if (c.dec > 1) p.ws.merge_list[off[4]] = s;
+    int full_off = 0;  // the sequence's first full chunk in the list
+#pragma unroll
+    for (int j = 0; j < kChunkClasses; ++j) {
+      if (j == c.cls) {
+        full_off = cls_off[j];
+        cls_off[j] += c.full;
+      }
+    }
     if (by_warp) {
       sq_cnt[s] = make_int4(c.dec, c.full, c.pf, c.n);
-      sq_off[s] = make_int4(off[0], off[1], off[2], off[3]);
-      sq_len[s] = make_int2(c.t0, c.q_s);
+      sq_off[s] = make_int4(off[0], full_off, off[2], off[3]);
+      sq_len[s] = make_int4(c.t0, c.q_s, c.mi, off[4]);
     } else {
-      for (int ch = 0; ch < c.dec; ++ch) write_dec_desc(p, s, c, off[0], off[1], off[2], tot[1], ch);
+      for (int ch = 0; ch < c.dec; ++ch) write_dec_desc(p, s, c, off[0], full_off, off[2], tot[1], ch);
       for (int qt = 0; qt < c.pf; ++qt) write_pf_desc(p, s, c, off[3], qt);
+      for (int k = 0; k < c.mi; ++k) write_merge_desc(p, s, c, off[0], off[4], k);
     }
     off[0] += c.dec;
     off[1] += c.full;
     off[2] += c.tail;
     off[3] += c.pf;
-    off[4] += c.dec > 1;
+    off[4] += c.mi;
   }
   if (by_warp) {
     __syncthreads();
     for (int s = warp; s < B; s += nw) {
       const int4 cn = sq_cnt[s], of = sq_off[s];
-      const int2 ln = sq_len[s];
-      const SeqCounts c{cn.x, cn.y, cn.x - cn.y, cn.z, cn.w, ln.x, ln.y};
+      const int4 ln = sq_len[s];
+      const SeqCounts c{cn.x, cn.y, cn.x - cn.y, cn.z, cn.w, ln.x, ln.y, 0, ln.z};
       for (int ch = lane; ch < c.dec; ch += 32) write_dec_desc(p, s, c, of.x, of.y, of.z, tot[1], ch);
       for (int qt = lane; qt < c.pf; qt += 32) write_pf_desc(p, s, c, of.w, qt);
+      for (int k = lane; k < c.mi; k += 32) write_merge_desc(p, s, c, of.x, ln.w, k);
     }
   }
   if (warp == 0) {

@@ -119,7 +119,7 @@ def test_workspace_size_is_host_only(lib):
     # block tables of 8 x 16 tokens: one split-KV chunk per sequence at most,
     # so at least one chunk output and log-sum-exp per (sequence, head)
     assert n.value >= 64 * 1 * 32 * (128 + 1) * 4
-    c = good(B=64, mb=4096)  # 65536-token tables: 128 chunks of 512 tokens
+    c = good(B=64, mb=4096)  # 65536-token tables: 512 chunks of 128 tokens
     k = ctypes.c_size_t(0)
     lib.pkv_attention_workspace_size(ctypes.byref(c["q"]), ctypes.byref(c["bt"]), ctypes.byref(c["kc"]),
                                      ctypes.byref(k))
