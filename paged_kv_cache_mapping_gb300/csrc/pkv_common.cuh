@@ -122,6 +122,24 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// The same with an L2 cache policy (createpolicy): data read once, such as
+// the K/V rows of a decode step, is marked evict-first, so that it does
+// not push out what the next kernels read again (tables, work lists,
+// split-KV partials).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel in the stream runs;
 // grid_dep_wait() blocks until that kernel has completed and its writes are

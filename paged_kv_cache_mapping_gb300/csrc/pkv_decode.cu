@@ -397,6 +397,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     const int tok = lane & 15;
     const bool is_v = lane >= 16;
     const int copy_b = HP * RowB;
+    const uint64_t pol = l2_evict_first_policy();  // each K/V row is read once per call
     int rec = 0, rphase = 0, slot = 0, phase = 0, fills = 0;
     for (;;) {
       if (!mbar_wait(rfull0 + 8 * rec, rphase, p.err)) {
@@ -452,13 +453,14 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, total);
       __syncwarp();
       if (joint) {
-        bulk_g2s(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, 2 * copy_b, full0 + 8 * slot);
+        bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, 2 * copy_b, full0 + 8 * slot,
+                      pol);
       } else if (act) {
         if (sl >= 0)
-          bulk_g2s(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, copy_b, full0 + 8 * slot);
+          bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, copy_b, full0 + 8 * slot, pol);
         if (KV == 2 && sl2 >= 0)
-          bulk_g2s(smem_u32(dst + copy_b), src + ((int64_t)sl2 * p.Hkv + head_off) * RowB, copy_b,
-                   full0 + 8 * slot);
+          bulk_g2s_hint(smem_u32(dst + copy_b), src + ((int64_t)sl2 * p.Hkv + head_off) * RowB, copy_b,
+                        full0 + 8 * slot, pol);
       }
       ++fills;
       if (++slot == NS) {
@@ -919,10 +921,11 @@ __global__ void __launch_bounds__(DecodeGeom<KV, D>::kThreads, 1) decode_kernel(
   // comes after the plan's kernel completed; so the plan's lists, and
   // everything written before the plan, are in place when the decode CTAs
   // start, and they read them through L2 (no stale L1 lines).  The prefill
-  // writes nothing the decode kernel reads.  Waiting for the prefill here,
-  // before the CTAs exit, makes this grid -- the last of the call --
-  // complete only after the prefill has.
-  if (p.dec_concurrent) grid_dep_wait();
+  // writes nothing the decode kernel reads.  CTA 0 waits for the prefill
+  // before it exits, which makes this grid -- the last of the call --
+  // complete only after the prefill has; the other CTAs leave as soon as
+  // their items are done, so that the next kernel's CTAs can take their SMs.
+  if (p.dec_concurrent && blockIdx.x == 0) grid_dep_wait();
 }
 
 // ---------------------------------------------------------------- launch

@@ -203,87 +203,114 @@ __device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigne
 // the last tokens first), KV head u % Hkv.  Key tiles are numbered across
 // the CTA's units (g); tile g uses K/V stage g % 3 and S / P buffer g % 2,
 // and signals o_done[g % 2] when its P V has finished.
+template <int D>
+__device__ __forceinline__ unsigned char* tc_smem() {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  return smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+}
+
+// What warp 0 reads once the previous kernel has completed, in one round
+// trip: the plan check and the prefill CTA count.
+struct TcStart {
+  int ok, active, n_units, pad;  // n_units: written by active CTAs after the check
+};
+
+// The barrier area (8-byte slots from Geo::kOffBar): mbarriers, the TMEM
+// address, the abort flag, the unit ring and its descriptors, the start
+// record.
+enum : int {
+  kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 5, kBarVFull = 8, kBarVEmpty = 11,
+  kBarSFull = 14, kBarPFull = 18, kBarODone = 20, kBarDrain = 23, kSlotTmem = 24, kSlotAbort = 25,
+  kBarUnitFull = 26, kBarUnitEmpty = 28, kSlotUnitRing = 30, kBarX = 32, kBarOFree = 40,
+  kOffUnitDesc = 384,  // bytes: PrefillDesc[2]
+  kOffStart = 448,     // bytes: TcStart
+};
+
+// Barriers, set up before the dependency wait (no global memory access),
+// and the tensor maps prefetched.
+template <int D>
+__device__ __forceinline__ void prefill_tc_setup(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                                 const CUtensorMap& tm_v) {
+  using Geo = TcGeom<D>;
+  unsigned char* smem = tc_smem<D>();
+  const uint32_t b0 = smem_u32(smem + Geo::kOffBar);
+  auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kBarSFull + b), 1);
+      mbar_init(bar(kBarPFull + b), 8);
+      mbar_init(bar(kBarODone + b), 1);
+      mbar_init(bar(kBarOFree + b), 8);
+      mbar_init(bar(kBarUnitFull + b), 1);
+      mbar_init(bar(kBarUnitEmpty + b), 10);  // the V producer, the MMA warp and the 8 softmax warps
+    }
+    mbar_init(bar(kBarDrain), 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(bar(kBarX + 2 * q), 2);
+      mbar_init(bar(kBarX + 2 * q + 1), 2);
+    }
+    *reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * kSlotAbort) = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane < 3) {
+    const CUtensorMap* m = lane == 0 ? &tm_q : lane == 1 ? &tm_k : &tm_v;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+  }
+}
+
 template <int D, typename OutT>
 __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                                const CUtensorMap& tm_v, int active) {
+                                                const CUtensorMap& tm_v, int active, int n_units,
+                                                int first_word) {
   using Geo = TcGeom<D>;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  unsigned char* smem = tc_smem<D>();
   const uint32_t sQ = smem_u32(smem + Geo::kOffQ);
   const uint32_t sK = smem_u32(smem + Geo::kOffK);
   const uint32_t sV = smem_u32(smem + Geo::kOffV);
   const uint32_t b0 = smem_u32(smem + Geo::kOffBar);
   auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
-  const uint32_t q_full = bar(0), q_empty = bar(1), drain = bar(23);
-  auto k_full = [&](int s) { return bar(2 + s); };
-  auto k_empty = [&](int s) { return bar(5 + s); };
-  auto v_full = [&](int s) { return bar(8 + s); };
-  auto v_empty = [&](int s) { return bar(11 + s); };
-  auto s_full = [&](int b) { return bar(14 + b); };
-  auto p_full = [&](int b) { return bar(18 + b); };
-  auto o_done = [&](int b) { return bar(20 + b); };
-  auto o_free = [&](int b) { return bar(40 + b); };  // O buffer b read out by the epilogue
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * 24);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 25);
+  const uint32_t q_full = bar(kBarQFull), q_empty = bar(kBarQEmpty), drain = bar(kBarDrain);
+  auto k_full = [&](int s) { return bar(kBarKFull + s); };
+  auto k_empty = [&](int s) { return bar(kBarKEmpty + s); };
+  auto v_full = [&](int s) { return bar(kBarVFull + s); };
+  auto v_empty = [&](int s) { return bar(kBarVEmpty + s); };
+  auto s_full = [&](int b) { return bar(kBarSFull + b); };
+  auto p_full = [&](int b) { return bar(kBarPFull + b); };
+  auto o_done = [&](int b) { return bar(kBarODone + b); };
+  auto o_free = [&](int b) { return bar(kBarOFree + b); };  // O buffer b read out by the epilogue
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * kSlotTmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * kSlotAbort);
   // work units: the TMA warp claims them and passes each index, with its
   // descriptor, to the other warps through a 2-slot ring (no warp reads a
   // descriptor from global memory on its way into a unit)
-  auto unit_full = [&](int b) { return bar(26 + b); };
-  auto unit_empty = [&](int b) { return bar(28 + b); };
-  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * 30);
-  PrefillDesc* unit_desc = reinterpret_cast<PrefillDesc*>(smem + Geo::kOffBar + 384);  // [2]
+  auto unit_full = [&](int b) { return bar(kBarUnitFull + b); };
+  auto unit_empty = [&](int b) { return bar(kBarUnitEmpty + b); };
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + Geo::kOffBar + 8 * kSlotUnitRing);
+  PrefillDesc* unit_desc = reinterpret_cast<PrefillDesc*>(smem + Geo::kOffBar + kOffUnitDesc);  // [2]
   // the two softmax warps of TMEM lane quarter q trade per-row values
   // through buffer b of xval, paired by barrier xbar(q, b)
-  auto xbar = [&](int q, int b) { return bar(32 + 2 * q + b); };
+  auto xbar = [&](int q, int b) { return bar(kBarX + 2 * q + b); };
   float* xval = reinterpret_cast<float*>(smem + Geo::kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the abort flag as one value for the whole warp (another warp may set it
   // between two lanes' reads)
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, *abort_flag != 0); };
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), 8);
-      mbar_init(o_done(b), 1);
-    }
-    mbar_init(o_free(0), 8);
-    mbar_init(o_free(1), 8);
-    mbar_init(drain, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(unit_full(b), 1);
-      mbar_init(unit_empty(b), 10);  // the V producer, the MMA warp and the 8 softmax warps
-    }
-    for (int q = 0; q < 4; ++q) {
-      mbar_init(xbar(q, 0), 2);
-      mbar_init(xbar(q, 1), 2);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
-                 "r"(Geo::kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tO = tmem + Geo::kColO;  // S / P buffers: columns 0 .. 2 * kTcKeys - 1; O buffers from here
 
   const int G = p.G, Hkv = p.Hkv;
   const int tq = p.pf_tq;  // query tokens per tile
-  const int n_units = p.ws.pf_off[p.B] * Hkv;
   const uint32_t q_box_bytes = (uint32_t)(Geo::kHalves * G * tq * 128);
 
   // Key tiles of a unit: from the first tile any of its rows sees (a sliding
@@ -369,7 +396,13 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     int u = blockIdx.x;
     for (; !aborted(); ++q_it) {
       PrefillDesc e{};
-      if (u < n_units) e = p.ws.pf_desc[u / Hkv];
+      if (q_it == 0) {  // word i of the first unit's descriptor is in lane i
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<int32_t*>(&e)[i] = __shfl_sync(0xffffffffu, first_word, i);
+      } else if (u < n_units) {
+        e = p.ws.pf_desc[u / Hkv];
+      }
       if (!publish(u, e)) { *abort_flag = 1; break; }
       if (u >= n_units) break;
       // claim c of the plan's runs names unit c mod n_units (see Workspace)
@@ -730,35 +763,84 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     if (ok && pend && !epilogue()) ok = false;  // the last unit's
     if (!ok) *abort_flag = 1;
   }
-  // ---- teardown: every MMA of this CTA has completed (its results were
-  // waited for above, or the MMA warp drained them), then free TMEM
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Geo::kTmemCols));
-  }
 }
 
 template <int D, typename OutT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using Geo = TcGeom<D>;
+  unsigned char* smem = tc_smem<D>();
+  prefill_tc_setup<D>(tm_q, tm_k, tm_v);
   // launched with programmatic dependent launch: wait for the previous
   // kernel (every thread, before any global access), then let the decode
   // kernel that follows launch and set up on the SMs this grid frees
   grid_dep_wait();
   launch_dependents();
-  if (plan_matches_warp(p)) {  // one answer for the whole grid
-    // the plan gives the prefill part of the SMs (the decode kernel takes
-    // the rest): the CTAs past that many leave at once, and the others
-    // take the units (first unit = CTA index, then claims)
-    int32_t n = 0;
-    if ((threadIdx.x & 31) == 0) n = __ldcg(p.ws.pf_ctas);
-    const int active = min(static_cast<int>(gridDim.x), __shfl_sync(0xffffffffu, n, 0));
-    if (static_cast<int>(blockIdx.x) < active) prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v, active);
-  } else if (threadIdx.x == 0) {
-    atomicOr(p.err, kErrPlan);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  TcStart* start = reinterpret_cast<TcStart*>(smem + Geo::kOffBar + kOffStart);
+  if (warp == 0) {
+    // one load per lane: the plan's signature (lanes 0 .. kPlanSig - 1) and
+    // its prefill CTA count (16); every CTA of every run reads these, so
+    // they are usually in L2
+    int32_t sig[kPlanSig];
+    plan_signature(p, sig);
+    int32_t want = 0;
+#pragma unroll
+    for (int i = 0; i < kPlanSig; ++i) want = lane == i ? sig[i] : want;
+    int32_t v = 0;
+    if (lane < kPlanSig) {
+      v = __ldcg(p.ws.sig + lane);
+    } else if (lane == 16) {
+      v = __ldcg(p.ws.pf_ctas);
+    }
+    const bool ok = __all_sync(0xffffffffu, lane >= kPlanSig || v == want);
+    const int n_ctas = __shfl_sync(0xffffffffu, v, 16);
+    if (lane == 0) {
+      start->ok = ok;
+      // the plan gives the prefill part of the SMs (the decode kernel takes
+      // the rest): the CTAs past that many leave at once
+      start->active = min(static_cast<int>(gridDim.x), n_ctas);
+    }
+  }
+  __syncthreads();
+  const int ok = start->ok, active = start->active;
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
+    return;
+  }
+  // the CTAs past the prefill's share leave at once (their SMs go to the
+  // decode kernel); the others allocate TMEM and take the units (first
+  // unit = CTA index, then claims)
+  if (static_cast<int>(blockIdx.x) >= active) return;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Geo::kOffBar + 8 * kSlotTmem);
+  // the unit count and the first unit's descriptor (unit = CTA index; the
+  // tile list has room for every CTA of the grid, whatever the plan holds)
+  // come in while TMEM is allocated
+  int first_word = 0, n_units = 0;
+  if (warp == 0) {
+    if (lane < 8) first_word = __ldcg(reinterpret_cast<const int32_t*>(p.ws.pf_desc + blockIdx.x / p.Hkv) + lane);
+    if (lane == 8) n_units = __ldcg(p.ws.pf_off + p.B) * p.Hkv;
+    n_units = __shfl_sync(0xffffffffu, n_units, 8);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "r"(Geo::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 0 && lane == 0) start->n_units = n_units;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  n_units = start->n_units;
+  prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v, active, n_units, first_word);
+  // ---- teardown: every MMA of this CTA has completed (its results were
+  // waited for, or the MMA warp drained them), then free TMEM
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tslot), "r"(Geo::kTmemCols));
   }
 }
 
