@@ -818,12 +818,16 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       l1 = l1 * al1 + (p1 + p3);
       m0 = mn0;
       m1 = mn1;
+      // the running max moves in few stages: most skip the rescale (a
+      // factor of exactly 1 leaves acc as it is)
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-      for (int i = 0; i < MT; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al1;
-        acc[i][2] *= al0;
-        acc[i][3] *= al1;
+        for (int i = 0; i < MT; ++i) {
+          acc[i][0] *= al0;
+          acc[i][1] *= al1;
+          acc[i][2] *= al0;
+          acc[i][3] *= al1;
+        }
       }
       // ---- O^T += V^T P : rows = d, cols = heads, k = tokens
       if constexpr (KV == 2) {
