@@ -574,7 +574,7 @@ pkv_status prepare(const pkv_tensor* q, const pkv_tensor* cu_seqlens_q, const pk
   const bool variant = p.soft_cap > 0.f || p.window_left >= 0;
   if (variant && c.prefill && !c.tc)
     return fail(PKV_ERR_UNSUPPORTED, "a soft cap or sliding window needs decode rows, or prefill rows on bf16 "
-                                     "caches with block sizes a multiple of 16 (max_q_len > 1 here)");
+                                     "or e4m3 caches with block sizes a multiple of 8 (max_q_len > 1 here)");
   p.pf_tq = c.tc ? pkv::prefill_tc_tokens_per_tile(G) : 0;
   p.path = !c.prefill ? 0 : (c.tc ? 2 : 1);
   // the decode kernel's KV heads per item: the plan cuts merge items by it

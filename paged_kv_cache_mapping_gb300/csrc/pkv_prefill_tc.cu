@@ -86,11 +86,12 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
-// K-major A, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128, N = n
-__host__ __device__ constexpr uint32_t umma_idesc(int n, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(kTcRows >> 4) << 24);
+// instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16
+// (f16 = false) or both f16, K-major A, B K-major (b_mn = 0) or MN-major
+// (b_mn = 1), M = 128, N = n
+__host__ __device__ constexpr uint32_t umma_idesc(int n, int b_mn, bool f16 = false) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
 }
 
 // The MMA and commit wrappers are executed by the whole (converged) warp
@@ -222,6 +223,7 @@ enum : int {
   kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 5, kBarVFull = 8, kBarVEmpty = 11,
   kBarSFull = 14, kBarPFull = 18, kBarODone = 20, kBarDrain = 23, kSlotTmem = 24, kSlotAbort = 25,
   kBarUnitFull = 26, kBarUnitEmpty = 28, kSlotUnitRing = 30, kBarX = 32, kBarOFree = 40,
+  kBarKsFull = 42, kBarVsFull = 44, kBarQConv = 47,  // e4m3 caches: tile copies landed, Q converted
   kOffUnitDesc = 384,  // bytes: PrefillDesc[2]
   kOffStart = 448,     // bytes: TcStart
 };
@@ -256,6 +258,9 @@ __device__ __forceinline__ void prefill_tc_setup(const CUtensorMap& tm_q, const 
       mbar_init(bar(kBarUnitEmpty + b), 10);  // the V producer, the MMA warp and the 8 softmax warps
     }
     mbar_init(bar(kBarDrain), 1);
+    for (int s = 0; s < kKStages; ++s) mbar_init(bar(kBarKsFull + s), 1);
+    for (int s = 0; s < kVStages; ++s) mbar_init(bar(kBarVsFull + s), 1);
+    mbar_init(bar(kBarQConv), 8);  // the softmax warps
     for (int q = 0; q < 4; ++q) {
       mbar_init(bar(kBarX + 2 * q), 2);
       mbar_init(bar(kBarX + 2 * q + 1), 2);
@@ -269,7 +274,7 @@ __device__ __forceinline__ void prefill_tc_setup(const CUtensorMap& tm_q, const 
   }
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool KV8>
 __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                                 const CUtensorMap& tm_v, int active, int n_units,
                                                 int first_word) {
@@ -301,6 +306,11 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   // the two softmax warps of TMEM lane quarter q trade per-row values
   // through buffer b of xval, paired by barrier xbar(q, b)
   auto xbar = [&](int q, int b) { return bar(kBarX + 2 * q + b); };
+  // e4m3 caches: a K / V tile's copies land in stage s (ks_full / vs_full)
+  // before its codes are converted; the MMAs wait for Q in f16 (q_conv)
+  auto ks_full = [&](int s) { return bar(kBarKsFull + s); };
+  auto vs_full = [&](int s) { return bar(kBarVsFull + s); };
+  const uint32_t q_conv = bar(kBarQConv);
   float* xval = reinterpret_cast<float*>(smem + Geo::kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the abort flag as one value for the whole warp (another warp may set it
@@ -320,31 +330,84 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     kt0 = first / kTcKeys;
     n_kt = (e.kv_end + kTcKeys - 1) / kTcKeys - kt0;
   };
-  // K or V tiles of one unit, one TMA box (16 keys x one d half) per lane;
-  // the block-table entry of the next tile is loaded while this one is
-  // issued.  claim: called (by the K producer) after the tile kt_claim is
-  // issued.
+  // e4m3 caches: a tile's codes (kTcKeys rows of D bytes) land at the end of
+  // its f16 stage and are converted in place into the 128-byte-swizzled
+  // layout the bf16 tiles have (16-byte chunk c of key r's row in d half h
+  // at h * kTcKeys * 128 + r * 128 + ((c ^ (r % 8)) * 16)); e4m3 -> f16 is
+  // exact.  Lane l reads 16 codes of one key (d 16 j .. 16 j + 15) and
+  // writes the two f16 chunks they make.  A written chunk only covers code
+  // rows read by this or an earlier loop step: with D = 128 a key's codes
+  // sit where its own d half 1 goes; with D = 64 output row r covers code
+  // rows 2 r - 128 and 2 r - 127 (r >= 64), never past the rows read so far.
+  constexpr int kStage8 = Geo::kKVBytes - kTcKeys * D;  // codes' offset in a stage
+  auto convert_kv = [&](uint32_t stage) {
+    constexpr int kCpr = D / 16;         // 16-code chunks per key
+    constexpr int kKeysPer = 32 / kCpr;  // keys per loop step
+    const int j = lane % kCpr, rr = lane / kCpr;
+    const int hh = j / 4, c0 = 2 * (j % 4);  // d half and first chunk of the 16 codes
+#pragma unroll 4
+    for (int r0 = 0; r0 < kTcKeys; r0 += kKeysPer) {
+      const int r = r0 + rr;
+      uint4 w;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                   : "r"(stage + kStage8 + r * D + 16 * j));
+      __syncwarp();
+      uint32_t f[8];
+      e4m3x4_to_f16(w.x, f[0], f[1]);
+      e4m3x4_to_f16(w.y, f[2], f[3]);
+      e4m3x4_to_f16(w.z, f[4], f[5]);
+      e4m3x4_to_f16(w.w, f[6], f[7]);
+      const uint32_t row = stage + hh * kTcKeys * 128 + r * 128;
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c0 ^ (r & 7)) << 4)), "r"(f[0]),
+                   "r"(f[1]), "r"(f[2]), "r"(f[3])
+                   : "memory");
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c0 + 1) ^ (r & 7)) << 4)), "r"(f[4]),
+                   "r"(f[5]), "r"(f[6]), "r"(f[7])
+                   : "memory");
+      __syncwarp();
+    }
+  };
+  // K or V tiles of one unit, one TMA box per issuing lane (bx keys x one d
+  // half, or bx keys x D e4m3 codes; bx = 16, or 8 for block sizes that are
+  // 8 mod 16, so that a box never crosses a block); the block-table entry of
+  // the next tile is loaded while this one is issued.  e4m3 tiles are
+  // converted one tile behind their copies.  claim: called (by the K
+  // producer) after the tile kt_claim is issued.
   auto stream_kv = [&](const PrefillDesc& e, int hk, int& g, bool is_v, int kt_claim, auto&& claim) -> bool {
     const int64_t n_slots = p.num_blocks * p.bs;
     const int32_t* bt_row = p.bt + (int64_t)e.s * p.bt_stride;
     int kt0, n_kt;
     unit_tiles(e, kt0, n_kt);
-    const int bi = lane & 7, h = (lane >> 3) & 1;  // keys 16 bi .. +15 of the tile, d half h
-    const bool issuer = lane < 8 * Geo::kHalves;
+    const int bx = (p.bs & 15) == 0 ? 16 : 8;
+    const int n_box = kTcKeys / bx;                       // boxes per d half (per tile for e4m3)
+    const int bi = lane % n_box;                          // keys bx bi .. bx bi + bx - 1 of the tile
+    const bool issuer = lane < n_box * (KV8 ? 1 : Geo::kHalves);
     constexpr int32_t kPast = INT32_MIN;  // a block past the sequence
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
     const uint32_t base = is_v ? sV : sK;
+    const int ns = is_v ? kVStages : kKStages;
     auto load_blk = [&](int kt) -> int32_t {
-      const int key0 = (kt0 + kt) * kTcKeys + 16 * bi;
+      const int key0 = (kt0 + kt) * kTcKeys + bx * bi;
       int32_t v = kPast;
       if (key0 < e.n) v = __ldg(bt_row + (p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs)));
       return v;
+    };
+    // e4m3: convert tile gg (waits for its copies), then hand it to the MMAs
+    auto convert = [&](int gg) -> bool {
+      const int st = gg % ns, ph = (gg / ns) & 1;
+      if (!mbar_wait_warp(is_v ? vs_full(st) : ks_full(st), ph, p.err)) return false;
+      convert_kv(base + st * Geo::kKVBytes);
+      fence_proxy_async_smem();  // the MMAs read the f16 tile through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(is_v ? v_full(st) : k_full(st));
+      return true;
     };
     int32_t blk = load_blk(0);
     for (int kt = 0; kt < n_kt; ++kt, ++g) {
       int32_t nxt = kPast;
       if (kt + 1 < n_kt) nxt = load_blk(kt + 1);
-      const int key0 = (kt0 + kt) * kTcKeys + 16 * bi;
+      const int key0 = (kt0 + kt) * kTcKeys + bx * bi;
       int slot = (int)n_slots;  // out of bounds: TMA fills zeros
       if ((uint32_t)blk < (uint32_t)p.num_blocks) {
         const int lb = p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs);
@@ -352,23 +415,39 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       } else if (blk != kPast) {
         atomicOr(p.err, kErrBlockRange);
       }
-      const int ns = is_v ? kVStages : kKStages;
       const int st = g % ns, ph = (g / ns) & 1;
-      const uint32_t full = is_v ? v_full(st) : k_full(st), empty = is_v ? v_empty(st) : k_empty(st);
+      const uint32_t empty = is_v ? v_empty(st) : k_empty(st);
       if (!mbar_wait_warp(empty, ph ^ 1, p.err)) return false;
-      if (lane == 0) mbar_arrive_expect_tx(full, Geo::kKVBytes);
-      __syncwarp();
-      if (issuer) tma_load_3d(base + st * Geo::kKVBytes + h * kTcKeys * 128 + bi * 2048, map, h * 64, hk, slot, full);
+      if constexpr (KV8) {
+        const uint32_t landed = is_v ? vs_full(st) : ks_full(st);
+        if (lane == 0) mbar_arrive_expect_tx(landed, kTcKeys * D);
+        __syncwarp();
+        if (issuer) tma_load_3d(base + st * Geo::kKVBytes + kStage8 + bi * bx * D, map, 0, hk, slot, landed);
+      } else {
+        const uint32_t full = is_v ? v_full(st) : k_full(st);
+        if (lane == 0) mbar_arrive_expect_tx(full, Geo::kKVBytes);
+        __syncwarp();
+        const int h = lane / n_box;  // d half
+        if (issuer) tma_load_3d(base + st * Geo::kKVBytes + h * kTcKeys * 128 + bi * bx * 128, map, h * 64, hk, slot,
+                                full);
+      }
       if (kt == kt_claim) claim();
+      if (KV8 && kt > 0 && !convert(g - 1)) return false;
       blk = nxt;
     }
+    if (KV8 && n_kt > 0 && !convert(g - 1)) return false;
     return true;
   };
   // giving up: let the copies a producer warp issued land before the CTA exits
   auto drain_copies = [&](int g, bool is_v) {
     const int ns = is_v ? kVStages : kKStages;
-    for (int k = g - 1; k >= 0 && k >= g - ns; --k)
-      mbar_wait_warp(is_v ? v_full(k % ns) : k_full(k % ns), (k / ns) & 1, p.err);
+    for (int k = g - 1; k >= 0 && k >= g - ns; --k) {
+      const int st = k % ns, ph = (k / ns) & 1;
+      if (KV8)
+        mbar_wait_warp(is_v ? vs_full(st) : ks_full(st), ph, p.err);
+      else
+        mbar_wait_warp(is_v ? v_full(st) : k_full(st), ph, p.err);
+    }
   };
 
   if (warp == 0) {
@@ -442,8 +521,8 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     if (aborted()) drain_copies(g, true);
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
-    constexpr uint32_t kIdQK = umma_idesc(kTcKeys, 0);
-    constexpr uint32_t kIdPV = umma_idesc(D, 1);
+    constexpr uint32_t kIdQK = umma_idesc(kTcKeys, 0, KV8);
+    constexpr uint32_t kIdPV = umma_idesc(D, 1, KV8);
     int g = 0, q_it = 0, ui = 0;
     bool ok = true;
     for (; ok && !aborted(); ++q_it) {
@@ -462,7 +541,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       unit_tiles(e, kt0, n_kt);
       const int ob = q_it & 1;  // O buffer of this unit (the epilogue may still read the other)
       const uint32_t tOu = tO + ob * 128;
-      ok = mbar_wait_warp(q_full, q_it & 1, p.err);
+      ok = mbar_wait_warp(KV8 ? q_conv : q_full, q_it & 1, p.err);
       // S[g % 2] = Q K^T for key tile g
       auto issue_qk = [&](int gg) -> bool {
         const int st = gg % kKStages, ph = (gg / kKStages) & 1, sb = gg & 1;
@@ -501,15 +580,16 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         if (!ok) break;
         tc_fence_after();
         {
-          // P hi in columns 0-63 of the buffer, P lo in 64-127: 16 keys are
-          // 8 columns; V is MN-major, 16 keys = 2048 bytes of each d half
+          // P hi in columns 0-63 of the buffer, P lo in 64-127 (e4m3 caches:
+          // P in f16, columns 0-63): 16 keys are 8 columns; V is MN-major, 16
+          // keys = 2048 bytes of each d half
           const uint32_t tp = tmem + pb * kTcKeys;
           const uint64_t dv = umma_desc(sV + st * Geo::kKVBytes, kTcKeys * 128, 1024);
           const uint32_t acc0 = t > 0;
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            umma_bf16_ta(tOu, tp + kk * 8, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);               // P hi
-            umma_bf16_ta(tOu, tp + kTcKeys / 2 + kk * 8, dv + kk * 128, kIdPV, 1);                 // P lo
+            umma_bf16_ta(tOu, tp + kk * 8, dv + kk * 128, kIdPV, kk > 0 ? 1u : acc0);  // P (hi)
+            if (!KV8) umma_bf16_ta(tOu, tp + kTcKeys / 2 + kk * 8, dv + kk * 128, kIdPV, 1);  // P lo
           }
           umma_commit(o_done(pb));
           umma_commit(v_empty(st));
@@ -614,6 +694,25 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       const int hk = u - (u / Hkv) * Hkv;
       const int ob = uc & 1;  // this unit's O buffer
       const uint32_t tOu = tO + ob * 128;
+      if constexpr (KV8) {
+        // the MMAs take f16 operands: Q (bf16, as its copy left it) to f16 in
+        // place, 16 bytes per step, before the unit's first Q K^T
+        if (!mbar_wait_warp(q_full, uc & 1, p.err)) { ok = false; break; }
+        const int tid = static_cast<int>(threadIdx.x) - 32 * kSoftmaxWarp0;
+#pragma unroll 2
+        for (int i = tid; i < Geo::kQBytes / 16; i += 32 * 8) {
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(sQ + 16 * i));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + 16 * i), "r"(bf16x2_to_f16x2(w.x)),
+                       "r"(bf16x2_to_f16x2(w.y)), "r"(bf16x2_to_f16x2(w.z)), "r"(bf16x2_to_f16x2(w.w))
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_conv);
+      }
       ++uc;
       int kt0, n_kt;
       unit_tiles(e, kt0, n_kt);
@@ -726,14 +825,18 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
             const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
             const unsigned long long pp = pk2(p0, p1);
             s2[w & 1] = add2(s2[w & 1], pp);
-            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-            hi[w] = __byte_perm(u0, u1, 0x7632);
-            float r0, r1;  // p - hi exactly: the truncated-away low bits
-            up2(sub2(pp, pk2(__uint_as_float(u0 & 0xFFFF0000u), __uint_as_float(u1 & 0xFFFF0000u))), r0, r1);
-            lo[w] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            if constexpr (KV8) {
+              hi[w] = pack_f16(p0, p1);  // f16 P (the e4m3 path's V is f16): nearest even
+            } else {
+              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+              hi[w] = __byte_perm(u0, u1, 0x7632);
+              float r0, r1;  // p - hi exactly: the truncated-away low bits
+              up2(sub2(pp, pk2(__uint_as_float(u0 & 0xFFFF0000u), __uint_as_float(u1 & 0xFFFF0000u))), r0, r1);
+              lo[w] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            }
           }
           tmem_st32(ts + 32 * half, hi);
-          tmem_st32(ts + kHalfKeys + 32 * half, lo);
+          if (!KV8) tmem_st32(ts + kHalfKeys + 32 * half, lo);
           float t0, t1, t2, t3;
           up2(s2[0], t0, t1);
           up2(s2[1], t2, t3);
@@ -765,7 +868,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   }
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool KV8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -833,7 +936,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   n_units = start->n_units;
-  prefill_tc_body<D, OutT>(p, tm_q, tm_k, tm_v, active, n_units, first_word);
+  prefill_tc_body<D, OutT, KV8>(p, tm_q, tm_k, tm_v, active, n_units, first_word);
   // ---- teardown: every MMA of this CTA has completed (its results were
   // waited for, or the MMA warp drained them), then free TMEM
   tc_fence_before();
@@ -877,16 +980,37 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t heads, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, typename OutT>
+// 3-D map of e4m3 codes {d, heads, rows} with a {D, 1, box_r} box (whole
+// rows of one head), no swizzle: the kernel converts them into the swizzled
+// f16 layout itself
+bool encode_3d_codes(CUtensorMap* m, const void* base, uint64_t d, uint64_t heads, uint64_t rows,
+                     uint64_t head_stride_b, uint64_t row_stride_b, uint32_t box_r) {
+  EncodeTiled fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {d, heads, rows};
+  const cuuint64_t strides[2] = {head_stride_b, row_stride_b};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, box_r};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, typename OutT, bool KV8>
 cudaError_t launch_tc(const AttnParams& p, int64_t max_units, int num_sms, cudaStream_t st) {
   using Geo = TcGeom<D>;
   CUtensorMap mq, mk, mv;
   const uint64_t n_slots = (uint64_t)p.num_blocks * (uint64_t)p.bs;
-  if (!encode_3d(&mq, p.q, D, p.Hq, p.T, (uint64_t)p.q_sh * 2, (uint64_t)p.q_st * 2, p.G, p.pf_tq) ||
-      !encode_3d(&mk, p.k_cache, D, p.Hkv, n_slots, (uint64_t)D * 2, (uint64_t)p.Hkv * D * 2, 1, 16) ||
-      !encode_3d(&mv, p.v_cache, D, p.Hkv, n_slots, (uint64_t)D * 2, (uint64_t)p.Hkv * D * 2, 1, 16))
+  const uint32_t bx = p.bs % 16 == 0 ? 16 : 8;  // keys per box: a box stays inside one block
+  if (!encode_3d(&mq, p.q, D, p.Hq, p.T, (uint64_t)p.q_sh * 2, (uint64_t)p.q_st * 2, p.G, p.pf_tq))
     return cudaErrorInvalidValue;
-  auto kern = prefill_tc_kernel<D, OutT>;
+  const bool kv_ok =
+      KV8 ? encode_3d_codes(&mk, p.k_cache, D, p.Hkv, n_slots, (uint64_t)D, (uint64_t)p.Hkv * D, bx) &&
+                encode_3d_codes(&mv, p.v_cache, D, p.Hkv, n_slots, (uint64_t)D, (uint64_t)p.Hkv * D, bx)
+          : encode_3d(&mk, p.k_cache, D, p.Hkv, n_slots, (uint64_t)D * 2, (uint64_t)p.Hkv * D * 2, 1, bx) &&
+                encode_3d(&mv, p.v_cache, D, p.Hkv, n_slots, (uint64_t)D * 2, (uint64_t)p.Hkv * D * 2, 1, bx);
+  if (!kv_ok) return cudaErrorInvalidValue;
+  auto kern = prefill_tc_kernel<D, OutT, KV8>;
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern), Geo::kSmem);
   if (e != cudaSuccess) return e;
   int64_t grid = num_sms;
@@ -898,17 +1022,18 @@ cudaError_t launch_tc(const AttnParams& p, int64_t max_units, int num_sms, cudaS
 }  // namespace
 
 bool prefill_tc_supported(int kv, int64_t D, int64_t bs, int64_t G) {
-  return kv == 1 && (D == 64 || D == 128) && bs % 16 == 0 && G >= 1 && G <= kTcRows;
+  return (kv == 1 || kv == 2) && (D == 64 || D == 128) && bs % 8 == 0 && G >= 1 && G <= kTcRows;
 }
 
 int prefill_tc_tokens_per_tile(int64_t G) { return (int)(kTcRows / G); }
 
 cudaError_t launch_prefill_tc(const AttnParams& p, int out_kind, int64_t max_units, int num_sms, cudaStream_t st) {
-  if (p.D == 128)
-    return out_kind ? launch_tc<128, __nv_bfloat16>(p, max_units, num_sms, st)
-                    : launch_tc<128, float>(p, max_units, num_sms, st);
-  return out_kind ? launch_tc<64, __nv_bfloat16>(p, max_units, num_sms, st)
-                  : launch_tc<64, float>(p, max_units, num_sms, st);
+#define PKV_TC(D, KV8)                                                          \
+  (out_kind ? launch_tc<D, __nv_bfloat16, KV8>(p, max_units, num_sms, st) \
+            : launch_tc<D, float, KV8>(p, max_units, num_sms, st))
+  if (p.kv_esize == 1) return p.D == 128 ? PKV_TC(128, true) : PKV_TC(64, true);
+  return p.D == 128 ? PKV_TC(128, false) : PKV_TC(64, false);
+#undef PKV_TC
 }
 
 }  // namespace pkv

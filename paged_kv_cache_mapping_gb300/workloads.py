@@ -301,19 +301,20 @@ def layout_sweep(block_size: int, contiguous: bool, B: int = 32, ctx: int = 2048
 
 def mixed_prefill(n_decode: int = 16, dec_ctx=(1024, 8192), chunk: int = 512,
                   prefix: int = 1024, block_size: int = 16, num_blocks: int = 8192,
-                  seed: int = 1004) -> Workload:
+                  seed: int = 1004, kv: str = "bf16") -> Workload:
     """Chunked-prefill step: n_decode decodes, then chunk A (chunk new tokens
     after a cached prefix whose blocks decodes 0 and 1 share) and chunk B
-    (chunk tokens, no prior context), packed decodes first."""
+    (chunk tokens, no prior context), packed decodes first.  kv: the cache
+    format ("bf16", or "e4m3" with per-tensor scales)."""
     dec = rng(seed, 4).integers(dec_ctx[0], dec_ctx[1] + 1, size=n_decode)
     lens = np.concatenate([dec, [prefix + chunk, chunk]]).astype(np.int32)
     ql = np.concatenate([np.ones(n_decode), [chunk, chunk]]).astype(np.int32)
     a = n_decode
     sharers = [s for s in (0, 1) if s < n_decode]
     mb = -(-max(dec_ctx[1], prefix + chunk) // block_size)
-    return build(f"mixed prefill {n_decode} decodes + 2x{chunk} chunks bf16",
+    return build(f"mixed prefill {n_decode} decodes + 2x{chunk} chunks {kv}",
                  Hq=32, Hkv=8, D=128, block_size=block_size, seq_lens=lens,
-                 q_lens=ql, src="bf16", kv="bf16", seed=seed,
+                 q_lens=ql, src="bf16", kv=kv, seed=seed,
                  num_blocks=num_blocks, max_blocks=mb,
                  shared=[(a, sharers, prefix)] if sharers and prefix else ())
 

@@ -174,8 +174,9 @@ def test_plan_and_run_validation(lib):
     assert lib.pkv_attention_run(*args, r(a["vc"]), 0.1, 1.0, 1.0, 0, r(_t(FAKE, F32, [4, 32, 64])), None, ws,
                                  1 << 30, None) == 1
     assert lib.pkv_attention_run(*args, r(a["vc"]), 0.1, 1.0, 1.0, 0, None, None, ws, 1 << 30, None) == 1
-    # a window on e4m3 caches with prefill rows (mma.sync prefill): unsupported, plan and run alike
-    b = good(kdt=E4M3)
+    # a window with prefill rows on a block size that is not a multiple of 8
+    # (the mma.sync prefill): unsupported, plan and run alike
+    b = good(kdt=E4M3, bs=12)
     var = pkv._Variant(0.0, 64)
     assert lib.pkv_attention_plan(r(b["q"]), r(b["cu"]), r(b["sl"]), r(b["bt"]), r(b["kc"]), 8, r(var), ws,
                                   1 << 30, None) == 2

@@ -56,6 +56,7 @@ def bench_step(wl, out_dtype):
 FULL = {
     "qwen3_4b_decode_b64": lambda: W.qwen3_4b_decode(),
     "mixed_prefill": lambda: W.mixed_prefill(),
+    "mixed_prefill_fp8": lambda: W.mixed_prefill(kv="e4m3"),
     "long_fp8_b8": lambda: W.long_fp8(),
     "lognormal_fp8_b256": lambda: W.lognormal_fp8(),
 }

@@ -168,16 +168,40 @@ def test_tensor_core_prefill_shapes(Hq, Hkv, D, bs):
     assert torch.equal(out16, bf16_rne_of(out))
 
 
-def test_tensor_core_prefill_layout_invariance_bitwise():
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_tensor_core_prefill_layout_invariance_bitwise(kv):
+    """Block sizes 8 and 24 take boxes of 8 slots, the others boxes of 16:
+    the tiles and their arithmetic are the same in every layout."""
     outs = []
-    for bs in (16, 32, 64):
+    for bs in (8, 16, 24, 32, 64):
         for contiguous in (False, True):
             wl = W.build("tc layout", Hq=32, Hkv=8, D=128, block_size=bs, seq_lens=[900, 333, 1],
-                         q_lens=[300, 333, 1], src="bf16", kv="bf16", seed=2011, contiguous=contiguous,
+                         q_lens=[300, 333, 1], src="bf16", kv=kv, seed=2011, contiguous=contiguous,
                          pool_slack=0.2)
             outs.append(run_gpu(wl)[1].cpu())
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+# Prefill rows on e4m3 caches and on block sizes that are 8 mod 16 go
+# through the tensor-core kernel too (codes converted to f16 in shared
+# memory, boxes of 8 slots); block sizes that are not multiples of 8 keep the
+# mma.sync kernel.  G 4, 4, 3, 8, 4, 3, 4, 4.
+@pytest.mark.parametrize("kv,Hq,Hkv,D,bs", [("e4m3", 32, 8, 128, 16), ("e4m3", 16, 4, 64, 8),
+                                            ("e4m3", 12, 4, 128, 24), ("e4m3", 64, 8, 64, 32),
+                                            ("bf16", 32, 8, 128, 8), ("bf16", 12, 4, 64, 24),
+                                            ("bf16", 32, 8, 128, 4), ("e4m3", 16, 4, 128, 12)])
+def test_prefill_cache_formats_and_block_sizes(kv, Hq, Hkv, D, bs):
+    wl = W.build("pf formats", Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seq_lens=[700, 130, 1, 300, 64],
+                 q_lens=[129, 130, 1, 45, 64], src="bf16", kv=kv, seed=2014, pool_slack=0.1)
+    ref, okc, ovc, _ = oracle.run_step(wl, nthreads=NT)
+    ds, out = run_gpu(wl)
+    assert oracle_caches_equal(ds, okc, ovc)
+    check_attention(out, ref, kv, f"prefill {kv} Hq{Hq} Hkv{Hkv} D{D} bs{bs}")
+    out16 = torch.empty(out.shape, dtype=torch.bfloat16, device=out.device)
+    ds.attention_only(out=out16)
+    torch.cuda.synchronize()
+    assert torch.equal(out16, bf16_rne_of(out))
 
 
 def test_fp8_d64_and_prefill():

@@ -27,18 +27,30 @@ def _mixed_tc():
                            num_blocks=1024, seed=2402)
 
 
-def _mixed_bs8():  # block size 8: the mma.sync prefill kernel
+def _mixed_bs8():  # block size 8: the tensor-core prefill with boxes of 8 slots
     return W.build("mixed bs8", Hq=32, Hkv=8, D=128, block_size=8, seq_lens=[700, 130, 1, 300],
                    q_lens=[1, 130, 1, 45], src="bf16", kv="bf16", seed=2403, pool_slack=0.1)
+
+
+def _mixed_bs4():  # block size 4: the mma.sync prefill kernel
+    return W.build("mixed bs4", Hq=32, Hkv=8, D=128, block_size=4, seq_lens=[700, 130, 1, 300],
+                   q_lens=[1, 130, 1, 45], src="bf16", kv="bf16", seed=2407, pool_slack=0.1)
+
+
+def _mixed_fp8():  # e4m3 caches: the tensor-core prefill on f16-converted tiles
+    return W.mixed_prefill(n_decode=5, dec_ctx=(300, 1400), chunk=200, prefix=160, block_size=16,
+                           num_blocks=1024, seed=2408, kv="e4m3")
 
 
 def _fp8():
     return W.lognormal_fp8(B=24, median=700, sigma=1.0, cap=6000, seed=2404)
 
 
-CASES = {"decode": (_decode, {}), "mixed_tc": (_mixed_tc, {}), "mixed_mma": (_mixed_bs8, {}),
-         "fp8": (_fp8, {}), "decode_window": (_decode, {"window_left": 300}),
-         "mixed_tc_window": (_mixed_tc, {"window_left": 100})}
+CASES = {"decode": (_decode, {}), "mixed_tc": (_mixed_tc, {}), "mixed_bs8": (_mixed_bs8, {}),
+         "mixed_mma": (_mixed_bs4, {}), "fp8": (_fp8, {}), "mixed_fp8": (_mixed_fp8, {}),
+         "decode_window": (_decode, {"window_left": 300}),
+         "mixed_tc_window": (_mixed_tc, {"window_left": 100}),
+         "mixed_fp8_window": (_mixed_fp8, {"window_left": 100})}
 
 
 def _layer_inputs(ds, layers, seed):

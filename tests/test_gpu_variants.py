@@ -1,6 +1,7 @@
 """Logits soft cap and sliding window (pkv_attention_ex) against the oracle
 with the same variant: decode rows (bf16 and e4m3, split across chunks, the
-window cutting into the first chunk) and tensor-core prefill rows."""
+window cutting into the first chunk) and tensor-core prefill rows (bf16 and
+e4m3 caches)."""
 import numpy as np
 import pytest
 import torch
@@ -28,6 +29,16 @@ def _mixed():
                            num_blocks=1024, seed=2403)
 
 
+def _mixed_fp8():
+    return W.mixed_prefill(n_decode=5, dec_ctx=(300, 1400), chunk=200, prefix=160, block_size=16,
+                           num_blocks=1024, seed=2406, kv="e4m3")
+
+
+def _fp8_pf_d64():
+    return W.build("fp8 pf", Hq=16, Hkv=4, D=64, block_size=8, seq_lens=[300, 77, 1, 900],
+                   q_lens=[120, 77, 1, 1], src="bf16", kv="e4m3", seed=2405, pool_slack=0.1)
+
+
 def _g16():
     return W.build("g16", Hq=64, Hkv=4, D=128, block_size=32, seq_lens=[1, 90, 700, 1500],
                    q_lens=[1, 1, 130, 1], src="bf16", kv="bf16", seed=2404, pool_slack=0.1)
@@ -37,9 +48,11 @@ def _g16():
     (_decode, 0.0, 300), (_decode, 20.0, -1), (_decode, 5.0, 1000), (_decode, 0.0, 0),
     (_fp8, 30.0, 500), (_fp8, 0.0, 129),
     (_mixed, 15.0, 200), (_mixed, 0.0, 64), (_mixed, 3.0, -1),
-    (_g16, 0.0, 100)],
+    (_g16, 0.0, 100),
+    (_mixed_fp8, 15.0, 200), (_mixed_fp8, 0.0, 64), (_fp8_pf_d64, 10.0, -1)],
     ids=["dec-w300", "dec-cap20", "dec-cap5-w1000", "dec-w0", "fp8-cap30-w500", "fp8-w129",
-         "mixed-cap15-w200", "mixed-w64", "mixed-cap3", "g16-w100"])
+         "mixed-cap15-w200", "mixed-w64", "mixed-cap3", "g16-w100",
+         "mixed-fp8-cap15-w200", "mixed-fp8-w64", "fp8-pf-d64-cap10"])
 def test_variant_matches_oracle(make, cap, window):
     wl = make()
     ref = oracle.run_step(wl, nthreads=NT, soft_cap=cap, window_left=window)[0]
@@ -58,8 +71,9 @@ def test_variants_outside_the_built_paths_are_refused():
     with pytest.raises(PkvError) as e:
         run_gpu(W.tiny(), window_left=3)  # fp32
     assert e.value.status == 2
-    fp8_prefill = W.build("fp8 pf", Hq=16, Hkv=4, D=64, block_size=8, seq_lens=[300, 77], q_lens=[120, 77],
+    # prefill rows on a block size that is not a multiple of 8 (the mma.sync kernel)
+    bs4_prefill = W.build("bs4 pf", Hq=16, Hkv=4, D=64, block_size=4, seq_lens=[300, 77], q_lens=[120, 77],
                           src="bf16", kv="e4m3", seed=2405, pool_slack=0.1)
     with pytest.raises(PkvError) as e:
-        run_gpu(fp8_prefill, soft_cap=10.0)
+        run_gpu(bs4_prefill, soft_cap=10.0)
     assert e.value.status == 2
