@@ -18,15 +18,26 @@
 // instructions there delays its MMA issues.  An M 128 x N 128 x K 16 MMA keeps
 // the tensor core at its full rate; N 64 would run at about two thirds.
 //
+// e4m3 caches ("How Easy Is It to Start Serving LLMs?", the FP8 KV cache
+// setting): the MMAs take f16 operands.  A K or V tile's codes land at the
+// end of its stage and the producer warp converts them in place to f16
+// (exact), in the swizzled layout a bf16 tile has; the softmax warps convert
+// each unit's Q tile from bf16 to f16 in place; P is one f16 part (P V runs
+// once).  The scales are folded into the exponent and the output, as in the
+// decode kernel.
+//
 // CTA (one per SM, persistent over tiles), 11 warps:
-//   warp 0   TMA producer: claims work units, loads the Q tile of each and
-//            its K tiles of 128 keys (8 boxes of 16 consecutive slots of one
-//            head per d half) into a 2-stage ring.
-//   warp 2   TMA producer of the V tiles, in its own 3-stage ring.
+//   warp 0   TMA producer: claims work units, loads the Q tile of each (two
+//            Q buffers: the next unit's Q arrives while this unit runs) and
+//            its K tiles of 128 keys (boxes of 16 consecutive slots of one
+//            head per d half, or of 8 for block sizes that are 8 mod 16, so
+//            that a box lies in one block) into a 2-stage ring.
+//   warp 2   TMA producer of the V tiles, in its own 2-stage ring.
 //            Keys past the sequence and bad block ids read out of bounds,
 //            which TMA fills with zeros.
 //   warp 1   MMA issuer (one thread) and owner of the TMEM allocation
-//            (S / P double-buffered in columns 0-255, O in 256-255+D).
+//            (S / P double-buffered in columns 0-255, O double-buffered in
+//            256-511: a unit's O is read out after the next unit's first tile).
 //            MMAs issued by one thread run in issue order, so the Q K^T that
 //            overwrites an S buffer is issued after the P V that reads it.
 //   warps 3-10  softmax, two threads per query row (a warp may only reach
@@ -40,7 +51,7 @@
 //            O in TMEM; at the end the partners add their sums and each
 //            writes half of O / l.  Q K^T of the next tile and P V of the
 //            previous one run on the tensor core meanwhile.
-// Block sizes must be multiples of 16 (a box of 16 keys lies in one block).
+// Block sizes must be multiples of 8.
 #include <cuda.h>
 
 #include <mutex>
@@ -53,7 +64,8 @@ namespace {
 constexpr int kTcRows = 128;    // query rows per tile (MMA M)
 constexpr int kTcKeys = 128;    // keys per key tile (MMA N of Q K^T, K of P V)
 constexpr int kKStages = 2;     // K ring depth
-constexpr int kVStages = 3;     // V ring depth (V is read later than K: it is requested earlier)
+constexpr int kVStages = 2;     // V ring depth
+constexpr int kQBufs = 2;       // Q tiles: the next unit's Q is loaded while this unit runs
 constexpr int kTcThreads = 352;  // 11 warps
 constexpr int kSoftmaxWarp0 = 3; // warps 3-10: two per TMEM lane quarter
 // A row's reference max moves only when a tile's max exceeds it by more than
@@ -67,7 +79,7 @@ struct TcGeom {
   static constexpr int kQBytes = kHalves * kTcRows * 128;
   static constexpr int kKVBytes = kHalves * kTcKeys * 128;   // one K or V tile
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   static constexpr int kOffX = kOffBar + 512;                 // row max / sum exchange [2][2][kTcRows]
@@ -220,10 +232,10 @@ struct TcStart {
 // address, the abort flag, the unit ring and its descriptors, the start
 // record.
 enum : int {
-  kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 5, kBarVFull = 8, kBarVEmpty = 11,
-  kBarSFull = 14, kBarPFull = 18, kBarODone = 20, kBarDrain = 23, kSlotTmem = 24, kSlotAbort = 25,
-  kBarUnitFull = 26, kBarUnitEmpty = 28, kSlotUnitRing = 30, kBarX = 32, kBarOFree = 40,
-  kBarKsFull = 42, kBarVsFull = 44, kBarQConv = 47,  // e4m3 caches: tile copies landed, Q converted
+  kBarQFull = 0, kBarQEmpty = 2, kBarKFull = 4, kBarKEmpty = 6, kBarVFull = 8, kBarVEmpty = 10,
+  kBarSFull = 12, kBarPFull = 14, kBarODone = 16, kBarDrain = 18, kSlotTmem = 19, kSlotAbort = 20,
+  kBarUnitFull = 21, kBarUnitEmpty = 23, kSlotUnitRing = 25, kBarX = 26, kBarOFree = 34,
+  kBarKsFull = 36, kBarVsFull = 38, kBarQConv = 40,  // e4m3 caches: tile copies landed, Q converted
   kOffUnitDesc = 384,  // bytes: PrefillDesc[2]
   kOffStart = 448,     // bytes: TcStart
 };
@@ -239,8 +251,11 @@ __device__ __forceinline__ void prefill_tc_setup(const CUtensorMap& tm_q, const 
   auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(bar(kBarQFull + b), 1);
+      mbar_init(bar(kBarQEmpty + b), 1);
+      mbar_init(bar(kBarQConv + b), 8);  // the softmax warps
+    }
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
       mbar_init(bar(kBarKEmpty + s), 1);
@@ -260,7 +275,6 @@ __device__ __forceinline__ void prefill_tc_setup(const CUtensorMap& tm_q, const 
     mbar_init(bar(kBarDrain), 1);
     for (int s = 0; s < kKStages; ++s) mbar_init(bar(kBarKsFull + s), 1);
     for (int s = 0; s < kVStages; ++s) mbar_init(bar(kBarVsFull + s), 1);
-    mbar_init(bar(kBarQConv), 8);  // the softmax warps
     for (int q = 0; q < 4; ++q) {
       mbar_init(bar(kBarX + 2 * q), 2);
       mbar_init(bar(kBarX + 2 * q + 1), 2);
@@ -285,7 +299,12 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   const uint32_t sV = smem_u32(smem + Geo::kOffV);
   const uint32_t b0 = smem_u32(smem + Geo::kOffBar);
   auto bar = [&](int i) -> uint32_t { return b0 + 8 * i; };
-  const uint32_t q_full = bar(kBarQFull), q_empty = bar(kBarQEmpty), drain = bar(kBarDrain);
+  // Q buffer b of unit parity b: filled (q_full), read by the unit's last
+  // Q K^T (q_empty)
+  auto q_full = [&](int b) { return bar(kBarQFull + b); };
+  auto q_empty = [&](int b) { return bar(kBarQEmpty + b); };
+  auto q_buf = [&](int b) { return sQ + b * Geo::kQBytes; };
+  const uint32_t drain = bar(kBarDrain);
   auto k_full = [&](int s) { return bar(kBarKFull + s); };
   auto k_empty = [&](int s) { return bar(kBarKEmpty + s); };
   auto v_full = [&](int s) { return bar(kBarVFull + s); };
@@ -310,7 +329,7 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
   // before its codes are converted; the MMAs wait for Q in f16 (q_conv)
   auto ks_full = [&](int s) { return bar(kBarKsFull + s); };
   auto vs_full = [&](int s) { return bar(kBarVsFull + s); };
-  const uint32_t q_conv = bar(kBarQConv);
+  auto q_conv = [&](int b) { return bar(kBarQConv + b); };
   float* xval = reinterpret_cast<float*>(smem + Geo::kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the abort flag as one value for the whole warp (another warp may set it
@@ -492,11 +511,12 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       int kt0, n_kt;
       unit_tiles(e, kt0, n_kt);
       const int hk = u - (u / Hkv) * Hkv;
-      if (!mbar_wait_warp(q_empty, (q_it & 1) ^ 1, p.err)) { *abort_flag = 1; break; }
+      const int qb = q_it & 1;  // this unit's Q buffer
+      if (!mbar_wait_warp(q_empty(qb), ((q_it >> 1) & 1) ^ 1, p.err)) { *abort_flag = 1; break; }
       if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, q_box_bytes);
+        mbar_arrive_expect_tx(q_full(qb), q_box_bytes);
         for (int h = 0; h < Geo::kHalves; ++h)
-          tma_load_3d(sQ + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full);
+          tma_load_3d(q_buf(qb) + h * kTcRows * 128, &tm_q, h * 64, hk * G, e.t0 + e.r0, q_full(qb));
       }
       if (!stream_kv(e, hk, g, false, max(0, n_kt - 3), claim)) { *abort_flag = 1; break; }
       int next = 0;
@@ -523,55 +543,71 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
     // ======================= MMA issuer =======================
     constexpr uint32_t kIdQK = umma_idesc(kTcKeys, 0, KV8);
     constexpr uint32_t kIdPV = umma_idesc(D, 1, KV8);
-    int g = 0, q_it = 0, ui = 0;
+    int g = 0, ui = 0;
     bool ok = true;
-    for (; ok && !aborted(); ++q_it) {
-      int u = n_units;
-      PrefillDesc e{};
-      ok = mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err);
-      if (ok) {
-        u = unit_ring[ui & 1];
-        e = unit_desc[ui & 1];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(unit_empty(ui & 1));
+    // S[gg % 2] = Q K^T for key tile gg (global numbering) against Q buffer qb
+    auto issue_qk = [&](int gg, int qb) -> bool {
+      const int st = gg % kKStages, ph = (gg / kKStages) & 1, sb = gg & 1;
+      // S buffer sb last held P of tile gg - 2, whose P V was issued before
+      // this Q K^T (issue order is execution order)
+      if (!mbar_wait_warp(k_full(st), ph, p.err)) return false;
+      tc_fence_after();
+      {
+        // a descriptor's start address is its low field (bytes >> 4): the
+        // k steps add constant offsets to one base descriptor per operand
+        const uint64_t dq = umma_desc(q_buf(qb), 16, 1024), dk = umma_desc(sK + st * Geo::kKVBytes, 16, 1024);
+#pragma unroll
+        for (int kb = 0; kb < D / 16; ++kb) {
+          const uint32_t kq = ((kb >> 2) * kTcRows * 128 + (kb & 3) * 32) >> 4;
+          const uint32_t kk = ((kb >> 2) * kTcKeys * 128 + (kb & 3) * 32) >> 4;
+          umma_bf16(tmem + sb * kTcKeys, dq + kq, dk + kk, kIdQK, kb > 0);
+        }
+        umma_commit(s_full(sb));
+        umma_commit(k_empty(st));
       }
+      __syncwarp();
+      return true;
+    };
+    // unit number q_it from the ring (u >= n_units: none left) and, for a
+    // real one, its Q tile ready in buffer q_it % 2
+    auto next_unit = [&](int q_it, int& u, PrefillDesc& e) -> bool {
+      u = n_units;
+      if (!mbar_wait_warp(unit_full(ui & 1), (ui >> 1) & 1, p.err)) return false;
+      u = unit_ring[ui & 1];
+      e = unit_desc[ui & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(unit_empty(ui & 1));
       ++ui;
-      if (!ok || u >= n_units) break;
+      if (u >= n_units) return true;
+      const int qb = q_it & 1;
+      return mbar_wait_warp(KV8 ? q_conv(qb) : q_full(qb), (q_it >> 1) & 1, p.err);
+    };
+    int u = n_units;
+    PrefillDesc e{};
+    ok = next_unit(0, u, e);
+    if (ok && u < n_units) ok = issue_qk(0, 0);  // the first unit's first tile (every unit has one)
+    for (int q_it = 0; ok && u < n_units && !aborted(); ++q_it) {
       int kt0, n_kt;
       unit_tiles(e, kt0, n_kt);
       const int ob = q_it & 1;  // O buffer of this unit (the epilogue may still read the other)
+      const int qb = q_it & 1;  // its Q buffer
       const uint32_t tOu = tO + ob * 128;
-      ok = mbar_wait_warp(KV8 ? q_conv : q_full, q_it & 1, p.err);
-      // S[g % 2] = Q K^T for key tile g
-      auto issue_qk = [&](int gg) -> bool {
-        const int st = gg % kKStages, ph = (gg / kKStages) & 1, sb = gg & 1;
-        // S buffer sb last held P of tile gg - 2, whose P V was issued before
-        // this Q K^T (issue order is execution order)
-        if (!mbar_wait_warp(k_full(st), ph, p.err)) return false;
-        tc_fence_after();
-        {
-          // a descriptor's start address is its low field (bytes >> 4): the
-          // k steps add constant offsets to one base descriptor per operand
-          const uint64_t dq = umma_desc(sQ, 16, 1024), dk = umma_desc(sK + st * Geo::kKVBytes, 16, 1024);
-#pragma unroll
-          for (int kb = 0; kb < D / 16; ++kb) {
-            const uint32_t kq = ((kb >> 2) * kTcRows * 128 + (kb & 3) * 32) >> 4;
-            const uint32_t kk = ((kb >> 2) * kTcKeys * 128 + (kb & 3) * 32) >> 4;
-            umma_bf16(tmem + sb * kTcKeys, dq + kq, dk + kk, kIdQK, kb > 0);
-          }
-          umma_commit(s_full(sb));
-          umma_commit(k_empty(st));
-        }
-        __syncwarp();
-        return true;
-      };
-      if (ok) ok = issue_qk(g);
+      int u2 = n_units;
+      PrefillDesc e2{};
       for (int t = 0; t < n_kt && ok; ++t) {
         const int gg = g + t;
         if (t + 1 < n_kt) {
-          ok = issue_qk(gg + 1);
+          ok = issue_qk(gg + 1, qb);
         } else {
-          umma_commit(q_empty);  // the unit's Q is no longer read
+          umma_commit(q_empty(qb));  // the unit's Q is no longer read
+          // the next unit's first Q K^T goes ahead of this unit's last P V,
+          // as within a unit, so that the softmax warps find its S ready
+          // (not with e4m3 caches: that Q is converted by the softmax warps
+          // after this unit's last P, which the P V below waits for)
+          if (!KV8) {
+            ok = next_unit(q_it + 1, u2, e2);
+            if (ok && u2 < n_units) ok = issue_qk(gg + 1, (q_it + 1) & 1);
+          }
         }
         if (!ok) break;
         const int st = gg % kVStages, ph = (gg / kVStages) & 1, pb = gg & 1;
@@ -597,6 +633,12 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
         __syncwarp();
       }
       g += n_kt;
+      if (KV8 && ok) {
+        ok = next_unit(q_it + 1, u2, e2);
+        if (ok && u2 < n_units) ok = issue_qk(g, (q_it + 1) & 1);
+      }
+      u = u2;
+      e = e2;
     }
     if (!ok || aborted()) {
       // giving up: every MMA issued so far must finish before TMEM is freed
@@ -697,21 +739,22 @@ __device__ __forceinline__ void prefill_tc_body(const AttnParams& p, const CUten
       if constexpr (KV8) {
         // the MMAs take f16 operands: Q (bf16, as its copy left it) to f16 in
         // place, 16 bytes per step, before the unit's first Q K^T
-        if (!mbar_wait_warp(q_full, uc & 1, p.err)) { ok = false; break; }
+        const int qb = uc & 1;
+        if (!mbar_wait_warp(q_full(qb), (uc >> 1) & 1, p.err)) { ok = false; break; }
         const int tid = static_cast<int>(threadIdx.x) - 32 * kSoftmaxWarp0;
 #pragma unroll 2
         for (int i = tid; i < Geo::kQBytes / 16; i += 32 * 8) {
           uint4 w;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                       : "r"(sQ + 16 * i));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + 16 * i), "r"(bf16x2_to_f16x2(w.x)),
+                       : "r"(q_buf(qb) + 16 * i));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_buf(qb) + 16 * i), "r"(bf16x2_to_f16x2(w.x)),
                        "r"(bf16x2_to_f16x2(w.y)), "r"(bf16x2_to_f16x2(w.z)), "r"(bf16x2_to_f16x2(w.w))
                        : "memory");
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(q_conv);
+        if (lane == 0) mbar_arrive(q_conv(qb));
       }
       ++uc;
       int kt0, n_kt;
