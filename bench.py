@@ -35,7 +35,7 @@ METRIC = "paged decode attention KV GB/s & % of GB300 HBM peak (Qwen3-4B heads, 
 UNIT = "GB/s"
 WORKLOADS = ("decode", "layout-bs1-scattered", "layout-bs1-contiguous", "layout-bs16-scattered",
              "layout-bs16-contiguous", "layout-bs64-scattered", "layout-bs64-contiguous", "mixed",
-             "mixed-chunks", "long-fp8", "lognormal-fp8")
+             "mixed-chunks", "mixed-fp8", "mixed-chunks-fp8", "long-fp8", "lognormal-fp8")
 DECODE_SOURCES = ["pkv_decode.cu", "pkv_pipeline.cuh", "pkv_common.cuh"]
 PREFILL_SOURCES = ["pkv_prefill_tc.cu", "pkv_common.cuh"]
 
@@ -606,27 +606,32 @@ def run_secondary(args, dev, clk):
     except Exception as e:  # reported, never fatal to the benchmark line
         out["layout"] = {"error": f"{type(e).__name__}: {e}"[:200]}
     calls = max(50, args.steps)
-    try:
-        wl = make_workload("mixed")
-        nb = step_bytes(wl)
-        ms = time_runs(wl, dev, calls, clk=clk)
-        chunks = wl.select([s for s in range(wl.B) if wl.q_lens[s] > 1])
-        fl = prefill_flops(wl)
-        ms_pf = time_runs(chunks, dev, calls, clk=clk)
-        rec = prefill_record()
-        out["mixed_prefill"] = {
-            "workload": wl.name, "call_us": round(ms * 1e3, 2),
-            "kv_gbs": round(nb["attention"] / (ms * 1e-3) / 1e9, 1),
-            "frac_hbm": round(nb["attention"] / (ms * 1e-3) / 1e9 / hbm, 4),
-            "prefill": {"bound": "tensor", "flops": fl, "call_us": round(ms_pf * 1e3, 2),
-                        "achieved": round(fl / (ms_pf * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-                        "peak": tflops, "frac": round(fl / (ms_pf * 1e-3) / 1e12 / tflops, 4),
-                        "frac_of_sustained": round(fl / (ms_pf * 1e-3) / 1e12 / tflops_sus, 4),
-                        "tensor_pipe_active": rec.get("sm__pipe_tensor_cycles_active_pct") if rec else None,
-                        "how": "the two prefill chunks alone (the tcgen05 prefill kernel and an empty decode "
-                               "launch), back-to-back runs; FLOPs = 4 Hq D per visible (query, key) pair"}}
-    except Exception as e:
-        out["mixed_prefill"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    for name, key in (("mixed", "mixed_prefill"), ("mixed-fp8", "mixed_prefill_fp8")):
+        try:
+            wl = make_workload(name)
+            nb = step_bytes(wl)
+            ms = time_runs(wl, dev, calls, clk=clk)
+            chunks = wl.select([s for s in range(wl.B) if wl.q_lens[s] > 1])
+            fl = prefill_flops(wl)
+            # the prefill alone moves with where its few MB of K/V land: the
+            # median over three fresh allocations
+            ms_pf = statistics.median(time_runs(chunks, dev, calls, clk=clk) for _ in range(3))
+            rec = prefill_record() if wl.kv == "bf16" else None
+            out[key] = {
+                "workload": wl.name, "call_us": round(ms * 1e3, 2),
+                "kv_gbs": round(nb["attention"] / (ms * 1e-3) / 1e9, 1),
+                "frac_hbm": round(nb["attention"] / (ms * 1e-3) / 1e9 / hbm, 4),
+                "prefill": {"bound": "tensor", "flops": fl, "call_us": round(ms_pf * 1e3, 2),
+                            "achieved": round(fl / (ms_pf * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                            "peak": tflops, "frac": round(fl / (ms_pf * 1e-3) / 1e12 / tflops, 4),
+                            "frac_of_sustained": round(fl / (ms_pf * 1e-3) / 1e12 / tflops_sus, 4),
+                            "tensor_pipe_active": rec.get("sm__pipe_tensor_cycles_active_pct") if rec else None,
+                            "how": "the two prefill chunks alone (the tcgen05 prefill kernel and an empty decode "
+                                   "launch), back-to-back runs, median of three allocations; FLOPs = 4 Hq D per "
+                                   "visible (query, key) pair" + ("; f16 MMAs (the bf16 peak applies)"
+                                                                  if wl.kv == "e4m3" else "")}}
+        except Exception as e:
+            out[key] = {"error": f"{type(e).__name__}: {e}"[:200]}
     for name in ("long-fp8", "lognormal-fp8"):
         try:
             wl = make_workload(name)
@@ -756,6 +761,11 @@ def make_workload(name, rank=0):
         return W.mixed_prefill(seed=1004 + off)
     if name == "mixed-chunks":  # the two prefill chunks of the mixed step alone
         wl = W.mixed_prefill(seed=1004 + off)
+        return wl.select([s for s in range(wl.B) if wl.q_lens[s] > 1])
+    if name == "mixed-fp8":  # the mixed step on e4m3 caches
+        return W.mixed_prefill(seed=1004 + off, kv="e4m3")
+    if name == "mixed-chunks-fp8":
+        wl = W.mixed_prefill(seed=1004 + off, kv="e4m3")
         return wl.select([s for s in range(wl.B) if wl.q_lens[s] > 1])
     if name == "long-fp8":
         return W.long_fp8(seed=1005 + off)
