@@ -11,13 +11,13 @@
 // Design (GB300):
 //   * A work item is (sequence, logical chunk, group of HP KV heads).  The
 //     chunk length depends only on N_s (128 * 2^k tokens, 256 * 2^k with an
-//     e4m3 cache, at most 128 chunks), so results depend neither on the
+//     e4m3 cache, at most 512 chunks), so results depend neither on the
 //     batch nor on the page layout
 //     ("How Easy Is It to Start Serving LLMs?", "3. Load balancing": long
 //     requests are split into chunks and a merge step stitches them).  The
-//     plan kernel lists the chunks once per call, every full chunk before
-//     the ragged last ones; persistent CTAs (one per SM) claim items from a
-//     global counter, so every SM stays busy to the end.
+//     plan lists the chunks once per model step, full chunks first (larger
+//     sizes first), ragged ones last; persistent CTAs (one per SM) claim
+//     items from a global counter, so every SM stays busy to the end.
 //   * One producer warp per CTA stages the chunk 16 logical tokens at a time:
 //     a token's K row for all HP heads of the group is HP * D contiguous
 //     elements of the cache (2 KB at D = 128, bf16, HP = 8), fetched with one
@@ -35,11 +35,11 @@
 //     converted exactly to f16 and P is f16.
 //   * A sequence of one chunk writes its output directly.  Otherwise each
 //     chunk writes its normalised output and log2-sum-exp2 to the workspace;
-//     once all the decode items are handed out, the same queue hands out one
-//     merge item per (split sequence, head group), which waits until the
-//     producers of the other CTAs report the sequence's chunks finished and
-//     combines them in chunk order -- the CTAs that run out of chunks merge
-//     while the others finish, with no second kernel launch.
+//     once all the decode items are handed out, the same queue hands out the
+//     merge items of each split sequence (query-head slices of a head group,
+//     R warps per head over ranges of the chunks), which wait until the other
+//     CTAs report the sequence's chunks finished and combine them in chunk
+//     order -- CTAs that run out of chunks merge while the others finish.
 #include <algorithm>
 
 #include "pkv_pipeline.cuh"

@@ -4,7 +4,7 @@
 //
 // Decode rows are cut into chunks whose length depends only on the
 // sequence's visible key count (128 * 2^k tokens, 256 * 2^k with an e4m3
-// cache, at most 128 chunks), so
+// cache, at most 512 chunks), so
 // results depend neither on the batch nor on the page layout ("How Easy Is
 // It to Start Serving LLMs?", "3. Load balancing": long requests are split
 // into chunks and a merge step stitches them).  Prefill rows are cut into
