@@ -238,10 +238,11 @@ PKV_API pkv_status pkv_attention(const pkv_tensor* q, const pkv_tensor* cu_seqle
  *   window_left      >= 0: the query at position p attends to keys
  *                    max(0, p - window_left) .. p; < 0 turns it off.
  *
- * Built for decode rows (bf16 and e4m3 caches) and for prefill rows on bf16
- * caches whose block size is a multiple of 16; other cases return
- * PKV_ERR_UNSUPPORTED.  variant == NULL is pkv_attention.  With a window, a
- * decode reads only the blocks its window touches.
+ * Built for decode rows and for prefill rows on caches whose block size is
+ * a multiple of 8 (bf16 and e4m3 caches alike); other cases (f32 caches,
+ * prefill rows on other block sizes) return PKV_ERR_UNSUPPORTED.
+ * variant == NULL is pkv_attention.  With a window, a decode reads only the
+ * blocks its window touches.
  */
 typedef struct {
   float logits_soft_cap;

@@ -216,8 +216,8 @@ cudaError_t launch_prefill(const AttnParams& p, int kv, int out_kind, int64_t ma
                            cudaStream_t st);
 cudaError_t launch_f32(const AttnParams& p, int out_kind, int64_t T, cudaStream_t st);
 
-// Tensor-core (tcgen05) prefill: bf16 caches, D 64 or 128, block size a
-// multiple of 16, G <= 128.
+// Tensor-core (tcgen05) prefill: bf16 or e4m3 caches, D 64 or 128, block
+// size a multiple of 8, G <= 128.
 bool prefill_tc_supported(int kv, int64_t D, int64_t bs, int64_t G);
 int prefill_tc_tokens_per_tile(int64_t G);
 cudaError_t launch_prefill_tc(const AttnParams& p, int out_kind, int64_t max_units, int num_sms, cudaStream_t st);
