@@ -70,17 +70,15 @@ struct StageRec {
 };
 
 // Shared memory of a decode CTA: the stage ring, the item ring, mbarriers.
-template <int KV, int D>
-__host__ __device__ inline int decode_tok_stride(int hp) { return hp * DecodeGeom<KV, D>::kRowB + 16; }
-// e4m3: tokens are staged in pairs, the two rows of a pair back to back (one
-// bulk copy of two adjacent slots fetches both) and 16 bytes of padding
-// between pairs.  bf16: one padded row per token.
+// Tokens are staged in pairs, the two rows of a pair back to back (one bulk
+// copy of two adjacent slots fetches both: the per-copy cost, not the bytes,
+// bounded an SM's rate with one copy per token row) and 16 bytes of padding
+// between pairs.
 template <int KV, int D>
 __host__ __device__ inline int decode_pair_stride(int hp) { return 2 * hp * DecodeGeom<KV, D>::kRowB + 16; }
 template <int KV, int D>
 __host__ __device__ inline int decode_half_bytes(int hp) {  // the K (or V) half of a stage
-  return KV == 2 ? (DecodeGeom<KV, D>::kST / 2) * decode_pair_stride<KV, D>(hp)
-                 : DecodeGeom<KV, D>::kST * decode_tok_stride<KV, D>(hp);
+  return (DecodeGeom<KV, D>::kST / 2) * decode_pair_stride<KV, D>(hp);
 }
 template <int KV, int D>
 __host__ __device__ inline int decode_stage_bytes(int hp) { return 2 * decode_half_bytes<KV, D>(hp); }
@@ -343,7 +341,6 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
   using Geo = DecodeGeom<KV, D>;
   constexpr int RowB = Geo::kRowB, ST = Geo::kST, MT = Geo::kMT, QRowB = Geo::kQRowB;
   const int HP = p.hp, NS = p.ns, G = p.G;
-  const int tokS = decode_tok_stride<KV, D>(HP);
   const int pairS = decode_pair_stride<KV, D>(HP);
   const int halfB = decode_half_bytes<KV, D>(HP);
   const int stageB = decode_stage_bytes<KV, D>(HP);
@@ -388,14 +385,16 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
 
   if (warp == HP) {
     // ======================= copy warp =======================
-    // Issues the K/V copies of each stage record: lane l copies token l % 16
-    // of the stage (K rows on lanes 0-15, V rows on lanes 16-31), all HP heads
-    // of the item in one 16-byte-aligned bulk copy.  It reads no global
-    // memory itself, so nothing but a free stage slot holds it up.
+    // Issues the K/V copies of each stage record, all HP heads of the item
+    // per token row, 16-byte-aligned bulk copies: lane l < 16 copies token
+    // pair l % 8 (K on lanes 0-7, V on 8-15), both rows in one copy when
+    // they are adjacent slots of one block.  Otherwise, with a bf16 cache
+    // lane l copies the pair's first row and lane l + 16 its second; with an
+    // e4m3 cache lane l copies both (the arrangement that measured fastest
+    // for each format).  It reads no global memory itself, so nothing but a
+    // free stage slot holds it up.
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
-    const int tok = lane & 15;
-    const bool is_v = lane >= 16;
     const int copy_b = HP * RowB;
     const uint64_t pol = l2_evict_first_policy();  // each K/V row is read once per call
     int rec = 0, rphase = 0, slot = 0, phase = 0, fills = 0;
@@ -404,13 +403,9 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
         flags[0] = 1;
         break;
       }
-      // bf16: lane l copies token l % 16 (K on lanes 0-15, V on 16-31).
-      // e4m3: lane l < 16 copies pair l % 8 (K on lanes 0-7, V on 8-15).
       const int q = lane & 7;
-      const bool pv = KV == 2 ? ((lane >> 3) & 1) != 0 : is_v;
-      const bool act = KV != 2 || lane < 16;
-      const int32_t sl = recs[rec].slot[KV == 2 ? 2 * q : tok];
-      const int32_t sl2 = KV == 2 ? recs[rec].slot[2 * q + 1] : -1;
+      const bool pv = ((lane >> 3) & 1) != 0;
+      const int32_t sl_a = recs[rec].slot[2 * q], sl_b = recs[rec].slot[2 * q + 1];
       const int head_off = recs[rec].head_off;
       mbar_arrive(rempty0 + 8 * rec);
       if (++rec == NR) {
@@ -423,43 +418,56 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
         break;
       }
       const char* src = pv ? vbase : kbase;
-      unsigned char* dst = smem + (size_t)slot * stageB + (pv ? halfB : 0) + (KV == 2 ? q * pairS : tok * tokS);
+      unsigned char* dst = smem + (size_t)slot * stageB + (pv ? halfB : 0) + q * pairS;
       // adjacent slots of one item covering every KV head are one contiguous run
-      const bool joint = KV == 2 && act && sl >= 0 && sl2 == sl + 1 && HP == p.Hkv;
+      const bool joint = sl_a >= 0 && sl_b == sl_a + 1 && HP == p.Hkv;
       int bytes = 0;
       bool zeroed = false;
-      if (act && !joint) {
-        if (sl < 0) {  // this token adds nothing: zeros keep the MMA inputs finite
-          uint4* z = reinterpret_cast<uint4*>(dst);
-          for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
-          zeroed = true;
-        } else {
-          bytes += copy_b;
+      auto zero_row = [&](unsigned char* row) {  // a token that adds nothing: zeros keep the MMA inputs finite
+        uint4* z = reinterpret_cast<uint4*>(row);
+        for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+        zeroed = true;
+      };
+      if constexpr (KV == 2) {
+        // lanes 0-15: the pair, or both of its rows one by one
+        const bool act = lane < 16;
+        if (act && !joint) {
+          if (sl_a < 0) zero_row(dst); else bytes += copy_b;
+          if (sl_b < 0) zero_row(dst + copy_b); else bytes += copy_b;
+        } else if (act) {
+          bytes = 2 * copy_b;
         }
-        if (KV == 2) {
-          if (sl2 < 0) {
-            uint4* z = reinterpret_cast<uint4*>(dst + copy_b);
-            for (int k = 0; k < copy_b / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
-            zeroed = true;
-          } else {
-            bytes += copy_b;
-          }
+        if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
+        const unsigned total = __reduce_add_sync(0xffffffffu, (unsigned)bytes);
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, total);
+        __syncwarp();
+        if (act && joint) {
+          bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl_a * p.Hkv + head_off) * RowB, 2 * copy_b,
+                        full0 + 8 * slot, pol);
+        } else if (act) {
+          if (sl_a >= 0)
+            bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl_a * p.Hkv + head_off) * RowB, copy_b, full0 + 8 * slot,
+                          pol);
+          if (sl_b >= 0)
+            bulk_g2s_hint(smem_u32(dst + copy_b), src + ((int64_t)sl_b * p.Hkv + head_off) * RowB, copy_b,
+                          full0 + 8 * slot, pol);
         }
-      } else if (joint) {
-        bytes = 2 * copy_b;
-      }
-      if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
-      const unsigned total = __reduce_add_sync(0xffffffffu, (unsigned)bytes);
-      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, total);
-      __syncwarp();
-      if (joint) {
-        bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, 2 * copy_b, full0 + 8 * slot,
-                      pol);
-      } else if (act) {
-        if (sl >= 0)
-          bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, copy_b, full0 + 8 * slot, pol);
-        if (KV == 2 && sl2 >= 0)
-          bulk_g2s_hint(smem_u32(dst + copy_b), src + ((int64_t)sl2 * p.Hkv + head_off) * RowB, copy_b,
+      } else {
+        // lanes 0-15: the pair or its first row; lanes 16-31: the second row
+        // of a pair that is not joint
+        const bool second = lane >= 16;
+        const bool act = !(second && joint);
+        const int32_t sl = second ? sl_b : sl_a;
+        if (second) dst += copy_b;
+        if (act) {
+          if (sl < 0) zero_row(dst); else bytes = joint ? 2 * copy_b : copy_b;
+        }
+        if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
+        const unsigned total = __reduce_add_sync(0xffffffffu, (unsigned)bytes);
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * slot, total);
+        __syncwarp();
+        if (bytes > 0)
+          bulk_g2s_hint(smem_u32(dst), src + ((int64_t)sl * p.Hkv + head_off) * RowB, (uint32_t)bytes,
                         full0 + 8 * slot, pol);
       }
       ++fills;
@@ -783,7 +791,8 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
           mma_f16(sc, a, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
         }
       } else {
-        const uint32_t aK = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * tokS + ((lane >> 4) & 1) * 16;
+        // MMA row r holds token 2 (r % 8) + r / 8, as on the e4m3 path
+        const uint32_t aK = sK + (lane & 7) * pairS + ((lane >> 3) & 1) * (HP * RowB) + ((lane >> 4) & 1) * 16;
 #pragma unroll
         for (int ks = 0; ks < MT; ++ks) {
           uint32_t a[4];
@@ -793,7 +802,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       }
       // ---- online softmax (base 2) per head column
       // the tokens of accumulator rows g4 and g4 + 8
-      const int tr0 = KV == 2 ? 2 * g4 : g4, tr1 = KV == 2 ? 2 * g4 + 1 : g4 + 8;
+      const int tr0 = 2 * g4, tr1 = 2 * g4 + 1;
       const bool v0 = j0 + tr0 < k1, v1 = j0 + tr1 < k1;
       if (p.soft_cap > 0.f) {  // soft cap: cap * tanh(s / cap), in base 2
 #pragma unroll
@@ -851,7 +860,8 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
         split_bf16(p0, p1, hi0, lo0);
         split_bf16(p2, p3, hi1, lo1);
         const uint32_t bh0 = movm_t(hi0), bh1 = movm_t(hi1), bl0 = movm_t(lo0), bl1 = movm_t(lo1);
-        const uint32_t aV = sV + ((lane & 7) + ((lane >> 4) & 1) * 8) * tokS + ((lane >> 3) & 1) * 16;
+        // k position j of the product is token 2 (j % 8) + j / 8, as in S
+        const uint32_t aV = sV + (lane & 7) * pairS + ((lane >> 4) & 1) * (HP * RowB) + ((lane >> 3) & 1) * 16;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t a[4];
