@@ -186,10 +186,13 @@ __device__ __forceinline__ long long prefill_key_tiles(const AttnParams& p, cons
 // tensor-core prefill and the decode kernel running beside it: a prefill
 // unit costs about kPfTileUs per 128-key tile (D = 128; half at D = 64)
 // plus kPfUnitUs of start and epilogue, a decode CTA streams about
-// kDecSmBytesPerUs of K/V, and all of them together at most kHbmBytesPerUs.
+// kDecSmBytesPerUs of K/V (bf16; kDecSmBytesPerUsFp8 with an e4m3 cache,
+// whose consumers do more work per byte), and all of them together at most
+// kHbmBytesPerUs.
 constexpr float kPfTileUs = 1.3f;
 constexpr float kPfUnitUs = 3.5f;
-constexpr float kDecSmBytesPerUs = 45e3f;
+constexpr float kDecSmBytesPerUs = 55e3f;
+constexpr float kDecSmBytesPerUsFp8 = 45e3f;
 constexpr float kHbmBytesPerUs = 6.0e6f;
 
 // Prefill CTAs for a call with the given prefill key tiles (per KV head) and
@@ -200,7 +203,8 @@ __device__ inline int prefill_cta_split(const AttnParams& p, long long pf_tiles,
   const int S = p.num_sms, lane = threadIdx.x & 31;
   if (dec_bytes == 0 || S < 2) return S;
   const float pf = (float)pf_tiles * (float)p.Hkv * kPfTileUs * (p.D / 128.f) + (float)pf_units * kPfUnitUs;
-  const float dec = (float)dec_bytes / kDecSmBytesPerUs, hbm = (float)dec_bytes / kHbmBytesPerUs;
+  const float rate = p.kv_esize == 1 ? kDecSmBytesPerUsFp8 : kDecSmBytesPerUs;
+  const float dec = (float)dec_bytes / rate, hbm = (float)dec_bytes / kHbmBytesPerUs;
   int best = S;
   float best_t = INFINITY;
   for (int P = lane + 1; P < S; P += 32) {
