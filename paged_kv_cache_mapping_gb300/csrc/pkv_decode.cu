@@ -61,12 +61,13 @@ struct DecodeGeom {
 __host__ __device__ inline int align16(int v) { return (v + 15) & ~15; }
 
 // One stage as the scheduler warp hands it to the copy warp: the cache slot
-// of each of its 16 tokens (-1: nothing to copy) and the first KV head of
-// the item (-1: no more stages).
+// of each of its 16 tokens (-1: nothing to copy), the first KV head of the
+// item (-1: no more stages) and the tokens that start a block (bit t).
 struct StageRec {
   int32_t slot[16];
   int32_t head_off;
-  int32_t pad[3];
+  uint32_t block_start;
+  int32_t pad[2];
 };
 
 // Shared memory of a decode CTA: the stage ring, the item ring, mbarriers.
@@ -388,7 +389,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     // Issues the K/V copies of each stage record, all HP heads of the item
     // per token row, 16-byte-aligned bulk copies: lane l < 16 copies token
     // pair l % 8 (K on lanes 0-7, V on 8-15), both rows in one copy when
-    // they are adjacent slots of one block.  Otherwise, with a bf16 cache
+    // they are adjacent slots of one block (block size 1: never).  Otherwise, with a bf16 cache
     // lane l copies the pair's first row and lane l + 16 its second; with an
     // e4m3 cache lane l copies both (the arrangement that measured fastest
     // for each format).  It reads no global memory itself, so nothing but a
@@ -407,6 +408,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       const bool pv = ((lane >> 3) & 1) != 0;
       const int32_t sl_a = recs[rec].slot[2 * q], sl_b = recs[rec].slot[2 * q + 1];
       const int head_off = recs[rec].head_off;
+      const uint32_t starts = recs[rec].block_start;
       mbar_arrive(rempty0 + 8 * rec);
       if (++rec == NR) {
         rec = 0;
@@ -419,8 +421,10 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       }
       const char* src = pv ? vbase : kbase;
       unsigned char* dst = smem + (size_t)slot * stageB + (pv ? halfB : 0) + q * pairS;
-      // adjacent slots of one item covering every KV head are one contiguous run
-      const bool joint = sl_a >= 0 && sl_b == sl_a + 1 && HP == p.Hkv;
+      // adjacent slots of one block, for an item covering every KV head, are
+      // one contiguous run; slots of adjacent blocks are not joined, so that
+      // the copies a stage takes do not depend on where its blocks lie
+      const bool joint = sl_a >= 0 && sl_b == sl_a + 1 && !((starts >> (2 * q + 1)) & 1u) && HP == p.Hkv;
       int bytes = 0;
       bool zeroed = false;
       auto zero_row = [&](unsigned char* row) {  // a token that adds nothing: zeros keep the MMA inputs finite
@@ -575,10 +579,13 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     };
     // Hands one record to the copy warp; every lane arrives, releasing its
     // own writes to the record.
-    auto put_record = [&](int tok_slot, bool writer, int head_off) -> bool {
+    auto put_record = [&](int tok_slot, bool writer, int head_off, uint32_t starts) -> bool {
       if (!mbar_wait(rempty0 + 8 * rec, rphase ^ 1, p.err)) return false;
       if (writer) recs[rec].slot[tok] = tok_slot;
-      if (lane == 0) recs[rec].head_off = head_off;
+      if (lane == 0) {
+        recs[rec].head_off = head_off;
+        recs[rec].block_start = starts;
+      }
       mbar_arrive(rfull0 + 8 * rec);
       if (++rec == NR) {
         rec = 0;
@@ -662,7 +669,9 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
 #pragma unroll
           for (int i = 0; i < GS; ++i) {
             if (gb + ST * i >= d.k1) break;
-            if (!put_record(sl[i >> 1], half == (i & 1), head_off)) {
+            // the stage's tokens at offset 0 of their block
+            const uint32_t m = __ballot_sync(0xffffffffu, off[i >> 1] == 0) >> (16 * (i & 1));
+            if (!put_record(sl[i >> 1], half == (i & 1), head_off, m & 0xffffu)) {
               ok = false;
               break;
             }
@@ -679,7 +688,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
     // ---- the end: the consumers' end marker, the copy warp's end record,
     // and the last item's split chunk reported once its slot comes back
     if (ok && !flags[0]) ok = publish(n_items, DecodeDesc{}, 0);
-    if (!put_record(-1, true, -1)) ok = false;
+    if (!put_record(-1, true, -1, 0u)) ok = false;
     if (ok && !flags[0]) {
       const int n_last = islot ? pub1 : pub0;  // the slot published before the end marker
       if (n_last > 0 && mbar_wait(iempty0 + 8 * islot, (n_last - 1) & 1, p.err)) retire(islot);
