@@ -18,13 +18,13 @@
 //     plan lists the chunks once per model step, full chunks first (larger
 //     sizes first), ragged ones last; persistent CTAs (one per SM) claim
 //     items from a global counter, so every SM stays busy to the end.
-//   * One producer warp per CTA stages the chunk 16 logical tokens at a time:
-//     a token's K row for all HP heads of the group is HP * D contiguous
-//     elements of the cache (2 KB at D = 128, bf16, HP = 8), fetched with one
+//   * A copy warp stages the chunk 16 logical tokens at a time: a token's K
+//     row for all HP heads of the group is HP * D contiguous elements (2 KB
+//     at D = 128, bf16, HP = 8), and two adjacent rows of one block go as one
 //     1-D bulk copy (TMA) that completes on the stage's mbarrier; V likewise.
-//     Whole-token copies keep the number of TMA requests low, which is what
-//     limits a TMA gather of small rows.  Block ids are fetched a group of
-//     16 stages ahead; the item's descriptor and query rows go through a
+//     Few, large copies keep the number of TMA requests low, which is what
+//     bounds an SM's rate.  A scheduler warp fetches block ids a group of 16
+//     stages ahead; the item's descriptor and query rows go through a
 //     two-slot item ring.  Every page is read once for all Hq/Hkv query heads.
 //   * Consumer warp h owns KV head h of the group for the whole chunk: S =
 //     K q^T and O^T += V^T P run on the tensor cores (mma.sync m16n8k16)
