@@ -141,14 +141,18 @@ def test_batch_composition_invariance_bitwise():
             assert torch.equal(o[6:7], o_all[0:1])
 
 
-@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 128), (16, 2, 64), (32, 2, 128), (12, 4, 64)])
-def test_head_shapes(Hq, Hkv, D):
-    """G = 1, 8, 16 (the latter through the tile path), 3; D = 64."""
+@pytest.mark.parametrize("Hq,Hkv,D,kv", [(8, 8, 128, "bf16"), (16, 2, 64, "bf16"), (32, 2, 128, "bf16"),
+                                         (12, 4, 64, "bf16"), (32, 16, 128, "bf16"), (32, 16, 128, "e4m3"),
+                                         (48, 16, 64, "e4m3")])
+def test_head_shapes(Hq, Hkv, D, kv):
+    """G = 1, 8, 16 (the latter through the tile path), 3; D = 64; and 16 KV
+    heads, where a decode item covers 8 of them, so a token pair's rows are
+    not one contiguous run and go as two copies."""
     wl = W.build("heads", Hq=Hq, Hkv=Hkv, D=D, block_size=16, seq_lens=[1, 90, 600, 1500],
-                 q_lens=[1, 1, 3, 1], src="bf16", kv="bf16", seed=2008, pool_slack=0.1)
+                 q_lens=[1, 1, 3, 1], src="bf16", kv=kv, seed=2008, pool_slack=0.1)
     ref = oracle.run_step(wl, nthreads=NT)[0]
     _, out = run_gpu(wl)
-    check_attention(out, ref, "bf16", f"Hq{Hq} Hkv{Hkv} D{D}")
+    check_attention(out, ref, kv, f"Hq{Hq} Hkv{Hkv} D{D} {kv}")
 
 
 # Prefill through the tensor-core (tcgen05) kernel: bf16 caches with block
