@@ -275,10 +275,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p) {
   }
   int off[5], tot[5];
   block_scan<5>(sum, off, tot);  // its barriers order the additions above
-  // full chunks: class j starts after every larger class
+  // full chunks: class j starts after every larger class.  When every
+  // sequence's chunks have one size (the usual case), that is the order of
+  // the sequences, which the scan above already gives.
   int cls_off[kChunkClasses], cls_tot[kChunkClasses];
-  block_scan<kChunkClasses>(cls, cls_off, cls_tot);
-  {
+  bool one_class = true;
+#pragma unroll
+  for (int j = 1; j < kChunkClasses; ++j) one_class = one_class && cls[j] == 0;
+  if (__syncthreads_and(one_class)) {
+#pragma unroll
+    for (int j = 0; j < kChunkClasses; ++j) cls_off[j] = j == 0 ? off[1] : 0;
+  } else {
+    block_scan<kChunkClasses>(cls, cls_off, cls_tot);
     int base = 0;
 #pragma unroll
     for (int j = kChunkClasses - 1; j >= 0; --j) {
