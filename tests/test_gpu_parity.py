@@ -155,6 +155,34 @@ def test_head_shapes(Hq, Hkv, D, kv):
     check_attention(out, ref, kv, f"Hq{Hq} Hkv{Hkv} D{D} {kv}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,kv,bs,q_lens", [
+    (32, 1, 128, "bf16", 16, [1, 1, 1, 1, 1]),     # G 32, decode rows only: tensor-core prefill, 4 tokens a tile
+    (32, 1, 128, "bf16", 16, [1, 1, 3, 1, 130]),
+    (128, 1, 64, "bf16", 16, [1, 1, 3, 1, 130]),   # G 128: one token a tile
+    (40, 2, 64, "e4m3", 16, [1, 1, 3, 1, 130]),    # G 20: 6 tokens, 120 of 128 rows
+    (96, 1, 64, "e4m3", 8, [1, 1, 3, 1, 130]),     # G 96: one token, 96 rows, boxes of 8 slots
+    (256, 1, 64, "bf16", 16, [1, 1, 3, 1, 130]),   # G 256: beyond a tile, the mma.sync prefill
+    (20, 4, 128, "bf16", 16, [1, 1, 1, 1, 1]),     # G 5 and 7: decode kernel, head columns 5-7 idle
+    (28, 4, 128, "e4m3", 16, [1, 1, 1, 1, 1]),
+])
+def test_wide_query_groups(Hq, Hkv, D, kv, bs, q_lens):
+    """Query groups wider than the decode kernel's eight head columns (the
+    rows of a sequence are its tokens times the group, as for a prefill
+    chunk), up to and past the 128 rows of a tensor-core tile, and groups
+    that fill only part of the decode kernel's columns."""
+    wl = W.build("wide groups", Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seq_lens=[1, 90, 600, 1500, 300],
+                 q_lens=q_lens, src="bf16", kv=kv, seed=2015, pool_slack=0.1)
+    ref, okc, ovc, _ = oracle.run_step(wl, nthreads=NT)
+    ds, out = run_gpu(wl)
+    assert oracle_caches_equal(ds, okc, ovc)
+    check_attention(out, ref, kv, f"Hq{Hq} Hkv{Hkv} D{D} {kv} bs{bs} q{q_lens}")
+    out16 = torch.empty(out.shape, dtype=torch.bfloat16, device=out.device)
+    ds.attention_only(out=out16)
+    torch.cuda.synchronize()
+    assert torch.equal(out16, bf16_rne_of(out))
+    assert pkv_device_errors() == 0
+
+
 # Prefill through the tensor-core (tcgen05) kernel: bf16 caches with block
 # sizes that are multiples of 16.  Chunks with and without a cached prefix,
 # token counts that are not multiples of a tile, a decode in the same batch.

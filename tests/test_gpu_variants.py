@@ -44,14 +44,21 @@ def _g16():
                    q_lens=[1, 1, 130, 1], src="bf16", kv="bf16", seed=2404, pool_slack=0.1)
 
 
+def _g32_decode():
+    # one KV head for 32 query heads: decode rows too wide for the decode
+    # kernel's head columns take the tensor-core prefill
+    return W.build("g32", Hq=32, Hkv=1, D=128, block_size=16, seq_lens=[1, 90, 700, 1500],
+                   q_lens=[1, 1, 1, 1], src="bf16", kv="bf16", seed=2407, pool_slack=0.1)
+
+
 @pytest.mark.parametrize("make,cap,window", [
     (_decode, 0.0, 300), (_decode, 20.0, -1), (_decode, 5.0, 1000), (_decode, 0.0, 0),
     (_fp8, 30.0, 500), (_fp8, 0.0, 129),
     (_mixed, 15.0, 200), (_mixed, 0.0, 64), (_mixed, 3.0, -1),
-    (_g16, 0.0, 100),
+    (_g16, 0.0, 100), (_g32_decode, 10.0, 300),
     (_mixed_fp8, 15.0, 200), (_mixed_fp8, 0.0, 64), (_fp8_pf_d64, 10.0, -1)],
     ids=["dec-w300", "dec-cap20", "dec-cap5-w1000", "dec-w0", "fp8-cap30-w500", "fp8-w129",
-         "mixed-cap15-w200", "mixed-w64", "mixed-cap3", "g16-w100",
+         "mixed-cap15-w200", "mixed-w64", "mixed-cap3", "g16-w100", "g32-dec-cap10-w300",
          "mixed-fp8-cap15-w200", "mixed-fp8-w64", "fp8-pf-d64-cap10"])
 def test_variant_matches_oracle(make, cap, window):
     wl = make()
@@ -76,4 +83,10 @@ def test_variants_outside_the_built_paths_are_refused():
                           src="bf16", kv="e4m3", seed=2405, pool_slack=0.1)
     with pytest.raises(PkvError) as e:
         run_gpu(bs4_prefill, soft_cap=10.0)
+    assert e.value.status == 2
+    # a query group wider than a tensor-core tile (G 256) also takes the mma.sync kernel
+    g256 = W.build("g256", Hq=256, Hkv=1, D=64, block_size=16, seq_lens=[300, 77], q_lens=[1, 1],
+                   src="bf16", kv="bf16", seed=2408, pool_slack=0.1)
+    with pytest.raises(PkvError) as e:
+        run_gpu(g256, window_left=50)
     assert e.value.status == 2
