@@ -32,7 +32,8 @@
 //     a head's softmax statistics live in one lane column and need no
 //     cross-warp combine.  P enters the PV product as a bf16 hi + lo pair
 //     (two MMAs; about 16 significant bits); with an e4m3 cache K and V are
-//     converted exactly to f16 and P is f16.
+//     converted exactly to f16 (V's codes come transposed from a byte-matrix
+//     load) and P is f16.
 //   * A sequence of one chunk writes its output directly.  Otherwise each
 //     chunk writes its normalised output and log2-sum-exp2 to the workspace;
 //     once all the decode items are handed out, the same queue hands out the
@@ -101,13 +102,20 @@ __host__ __device__ inline size_t decode_smem(int hp, int ns, int G) {
          DecodeGeom<KV, D>::kRecs * sizeof(StageRec) + (2 * ns + 6 + 2 * DecodeGeom<KV, D>::kRecs) * 8 + 16;
 }
 
+// Two 16 x 16 byte matrices, transposed on the way: lanes 0-15 give the
+// addresses of matrix 0's rows, lanes 16-31 those of matrix 1.  Lane 4g + t
+// receives, of matrix 0, column g of rows 4t .. 4t+3 (r0, row 4t in the low
+// byte) and column g + 8 of the same rows (r1); r2, r3 likewise of matrix 1.
+__device__ __forceinline__ void ldsm_b8_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                             uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // Output column d of accumulator tile mt, half (0: row g, 1: row g + 8).
-template <int KV>
 __device__ __forceinline__ int acc_d(int mt, int half, int g) {
-  if constexpr (KV == 2)
-    return 16 * mt + 4 * (g >> 1) + (g & 1) + 2 * half;  // permuted d of the e4m3 path
-  else
-    return 16 * mt + g + 8 * half;
+  return 16 * mt + g + 8 * half;
 }
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
@@ -849,18 +857,23 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       }
       // ---- O^T += V^T P : rows = d, cols = heads, k = tokens
       if constexpr (KV == 2) {
+        // k positions 2t, 2t + 1, 2t + 8, 2t + 9 of the product are tokens
+        // 4t, 4t + 2, 4t + 1, 4t + 3 (the transposed P below); a transposing
+        // byte load of V rows in the order 4t, 4t + 2, 4t + 1, 4t + 3 (bits 0
+        // and 1 of the row index swapped) gives each lane its codes in that
+        // order, d = 16 mt + g (and + 8) down the rows
         const uint32_t b0 = movm_t(pack_f16(p0, p1)), b1 = movm_t(pack_f16(p2, p3));
-        const uint32_t aV = sV + (lane & 7) * pairS + ((lane >> 3) & 1) * (HP * RowB) + (lane >> 4) * 16;
+        const int vr = lane & 15;
+        const uint32_t aV = sV + ((vr >> 2) * 2 + (vr & 1)) * pairS + ((vr >> 1) & 1) * (HP * RowB) + (lane >> 4) * 16;
 #pragma unroll
         for (int cp = 0; cp < MT / 2; ++cp) {
           uint32_t w0, w1, w2, w3;
-          ldsm_x4(aV + 32 * cp, w0, w1, w2, w3);
+          ldsm_b8_x2_t(aV + 32 * cp, w0, w1, w2, w3);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t x0t, x1t, x0b, x1b;
-            e4m3x4_to_f16(hh ? w2 : w0, x0t, x1t);
-            e4m3x4_to_f16(hh ? w3 : w1, x0b, x1b);
-            const uint32_t a[4] = {movm_t(x0t), movm_t(x1t), movm_t(x0b), movm_t(x1b)};
+            uint32_t a[4];
+            e4m3x4_to_f16(hh ? w2 : w0, a[0], a[2]);
+            e4m3x4_to_f16(hh ? w3 : w1, a[1], a[3]);
             mma_f16(acc[2 * cp + hh], a, b0, b1);
           }
         }
@@ -901,7 +914,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int dd = acc_d<KV>(mt, half, g4);
+          const int dd = acc_d(mt, half, g4);
           if (c0 < G) store1(static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + c0) * p.o_sh + dd,
                              acc[mt][2 * half] * r0);
           if (c1 < G) store1(static_cast<OutT*>(p.out) + (int64_t)t * p.o_st + (int64_t)(hq0 + c1) * p.o_sh + dd,
@@ -914,7 +927,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int dd = acc_d<KV>(mt, half, g4);
+          const int dd = acc_d(mt, half, g4);
           if (c0 < G) po[(int64_t)(hq0 + c0) * D + dd] = acc[mt][2 * half] * r0;
           if (c1 < G) po[(int64_t)(hq0 + c1) * D + dd] = acc[mt][2 * half + 1] * r1;
         }
