@@ -351,6 +351,11 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
   constexpr int RowB = Geo::kRowB, ST = Geo::kST, MT = Geo::kMT, QRowB = Geo::kQRowB;
   const int HP = p.hp, NS = p.ns, G = p.G;
   const int pairS = decode_pair_stride<KV, D>(HP);
+  // e4m3: MMA rows 8-15 take the odd tokens of pairs rot, rot + 1, .. (mod
+  // 8), so that the byte-matrix V loads below read eight different bank
+  // groups per eight rows; rot = 4 where a pair's two rows sit a multiple
+  // of 128 bytes apart (their banks coincide), else 0
+  const int rot = KV == 2 && ((HP * RowB) & 127) == 0 ? 4 : 0;
   const int halfB = decode_half_bytes<KV, D>(HP);
   const int stageB = decode_stage_bytes<KV, D>(HP);
   const int itemB = decode_item_bytes<KV, D>(HP, G);
@@ -792,9 +797,11 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       // ---- S = K q^T : rows = 16 tokens, cols = heads
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (KV == 2) {
-        // MMA row r holds token 2 (r % 8) + r / 8: each 8-row matrix reads 8
-        // different pairs, in 8 different bank groups
-        const uint32_t aK = sK + (lane & 7) * pairS + ((lane >> 3) & 1) * (HP * RowB) + (lane >> 4) * 16;
+        // MMA row r < 8 holds token 2r, row 8 + r the odd token of pair
+        // (r + rot) % 8: each 8-row matrix reads 8 different pairs, in 8
+        // different bank groups
+        const int kodd = (lane >> 3) & 1;
+        const uint32_t aK = sK + (((lane & 7) + kodd * rot) & 7) * pairS + kodd * (HP * RowB) + (lane >> 4) * 16;
 #pragma unroll
         for (int kp = 0; kp < MT / 2; ++kp) {
           uint32_t w0, w1, w2, w3;
@@ -819,7 +826,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       }
       // ---- online softmax (base 2) per head column
       // the tokens of accumulator rows g4 and g4 + 8
-      const int tr0 = 2 * g4, tr1 = 2 * g4 + 1;
+      const int tr0 = 2 * g4, tr1 = 2 * ((g4 + rot) & 7) + 1;
       const bool v0 = j0 + tr0 < k1, v1 = j0 + tr1 < k1;
       if (p.soft_cap > 0.f) {  // soft cap: cap * tanh(s / cap), in base 2
 #pragma unroll
@@ -857,14 +864,17 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
       }
       // ---- O^T += V^T P : rows = d, cols = heads, k = tokens
       if constexpr (KV == 2) {
-        // k positions 2t, 2t + 1, 2t + 8, 2t + 9 of the product are tokens
-        // 4t, 4t + 2, 4t + 1, 4t + 3 (the transposed P below); a transposing
-        // byte load of V rows in the order 4t, 4t + 2, 4t + 1, 4t + 3 (bits 0
-        // and 1 of the row index swapped) gives each lane its codes in that
-        // order, d = 16 mt + g (and + 8) down the rows
+        // k positions 2t, 2t + 1 of the product are the tokens of MMA rows
+        // 2t, 2t + 1 (tokens 4t, 4t + 2) and k positions 2t + 8, 2t + 9 those
+        // of rows 2t + 8, 2t + 9 (the odd tokens of pairs 2t + rot, 2t + 1 +
+        // rot, mod 8), as the transposed P below has them; a transposing
+        // byte load of the V rows of those four tokens, in that order, as
+        // source rows 4t .. 4t + 3 gives each lane its codes in k order,
+        // d = 16 mt + g (and + 8) down the rows
         const uint32_t b0 = movm_t(pack_f16(p0, p1)), b1 = movm_t(pack_f16(p2, p3));
-        const int vr = lane & 15;
-        const uint32_t aV = sV + ((vr >> 2) * 2 + (vr & 1)) * pairS + ((vr >> 1) & 1) * (HP * RowB) + (lane >> 4) * 16;
+        const int vr = lane & 15, vb = vr & 3, vt = vr >> 2;
+        const int vpair = vb < 2 ? 2 * vt + vb : (2 * vt + vb - 2 + rot) & 7;
+        const uint32_t aV = sV + vpair * pairS + (vb >> 1) * (HP * RowB) + (lane >> 4) * 16;
 #pragma unroll
         for (int cp = 0; cp < MT / 2; ++cp) {
           uint32_t w0, w1, w2, w3;
