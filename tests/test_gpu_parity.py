@@ -143,11 +143,14 @@ def test_batch_composition_invariance_bitwise():
 
 @pytest.mark.parametrize("Hq,Hkv,D,kv", [(8, 8, 128, "bf16"), (16, 2, 64, "bf16"), (32, 2, 128, "bf16"),
                                          (12, 4, 64, "bf16"), (32, 16, 128, "bf16"), (32, 16, 128, "e4m3"),
-                                         (48, 16, 64, "e4m3")])
+                                         (48, 16, 64, "e4m3"), (12, 3, 64, "e4m3"), (8, 1, 64, "e4m3"),
+                                         (20, 5, 128, "e4m3")])
 def test_head_shapes(Hq, Hkv, D, kv):
-    """G = 1, 8, 16 (the latter through the tile path), 3; D = 64; and 16 KV
+    """G = 1, 8, 16 (the latter through the tile path), 3; D = 64; 16 KV
     heads, where a decode item covers 8 of them, so a token pair's rows are
-    not one contiguous run and go as two copies."""
+    not one contiguous run and go as two copies; and e4m3 items of 3, 1 and 5
+    KV heads (at D = 64 the two rows of a pair then sit 64 bytes off a
+    128-byte multiple apart and the MMA rows keep their unrotated order)."""
     wl = W.build("heads", Hq=Hq, Hkv=Hkv, D=D, block_size=16, seq_lens=[1, 90, 600, 1500],
                  q_lens=[1, 1, 3, 1], src="bf16", kv=kv, seed=2008, pool_slack=0.1)
     ref = oracle.run_step(wl, nthreads=NT)[0]
