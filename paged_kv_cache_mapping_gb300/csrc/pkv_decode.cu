@@ -815,7 +815,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p) {
           mma_f16(sc, a, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
         }
       } else {
-        // MMA row r holds token 2 (r % 8) + r / 8, as on the e4m3 path
+        // MMA row r holds token 2 (r % 8) + r / 8 (the e4m3 order with rot 0)
         const uint32_t aK = sK + (lane & 7) * pairS + ((lane >> 3) & 1) * (HP * RowB) + ((lane >> 4) & 1) * 16;
 #pragma unroll
         for (int ks = 0; ks < MT; ++ks) {
